@@ -1,0 +1,388 @@
+#!/usr/bin/env python3
+"""Benchmark of the NABLA hot path on GB300: mask build + block-sparse attention.
+
+One step = nabla_build_mask (pool -> pooled map -> select/CSR) followed by
+nabla_attn_fwd over the kept 64x64 blocks, on one batch of the seeded synthetic
+workload (default: the 720p-like latent, B=1, h=24, D=128, S=98,304, thr=0.9,
+STA half-widths (3,1,1)).  Prints ONE JSON line (rank 0).
+
+  value       kept-block attention TFLOP/s over the whole step (mask build
+              included), inputs resident in HBM, CUDA-event timed;
+  e2e         the same metric with q/k/v copied from pinned host memory and o
+              copied back inside the timed region;
+  roofline    the dominant kernel (attention) against the measured bf16 peak;
+              mask_roofline: the mask builder against measured HBM bandwidth;
+  cpu_baseline the fp64 oracle on a bounded sample, timed on the host cores.
+`--impl reference` times the oracle itself (the reference arm of this repo).
+Multi-GPU (torchrun): independent replicas, one per GPU, max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_attention_nablat_gb300 import workloads as W  # noqa: E402
+
+METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM GB/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def mask_bytes(w, total_kept_blocks: int) -> float:
+    """Algorithmic bytes of one mask build: read q and k once, read the STA
+    window once, write kv_nb and the kept kv_inds entries."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return (2.0 * w.B * w.S * w.h * w.D * esz + w.s1 * w.s1 + 4.0 * w.B * w.h * w.s1
+            + 4.0 * total_kept_blocks)
+
+
+def attn_flops(w, total_kept_blocks: int) -> float:
+    """QK^T and PV over each kept 64x64 block: 2 * 2 * 64 * 64 * D FLOP per block."""
+    return 4.0 * 64 * 64 * w.D * total_kept_blocks
+
+
+def dense_flops(w) -> float:
+    return 4.0 * w.B * w.h * w.S * w.S * w.D
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id(dev) -> str:
+    """nvidia-smi selector of a torch device (its UUID; nvidia-smi does not follow
+    CUDA_VISIBLE_DEVICES numbering)."""
+    import torch
+
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid is not None:
+        u = str(uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    return str(dev.index or 0)
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def oracle_sample(w, data, sta, thr, kv_nb=None, kv_inds=None, n_qblocks=8, seed=0):
+    """Time the fp64 oracle on a bounded sample of the workload: the mask builder
+    for one (batch, head) and the attention for n_qblocks query blocks.  Returns
+    (kept FLOPs covered, seconds, description)."""
+    from oracle import nabla_oracle as O
+
+    qf = W.as_float(data["q"][:, :, :1])
+    kf = W.as_float(data["k"][:, :, :1])
+    t0 = time.perf_counter()
+    r = O.build_mask(qf[:1], kf[:1], sta, thr)
+    t_mask = time.perf_counter() - t0
+    nb = r["kv_nb"] if kv_nb is None else kv_nb[:1, :1]
+    inds = r["kv_inds"] if kv_inds is None else kv_inds[:1, :1]
+    rng = np.random.default_rng(seed)
+    qb = sorted({int(x) for x in rng.integers(0, w.s1, n_qblocks)})
+    vf = W.as_float(data["v"][:1, :, :1])
+    t0 = time.perf_counter()
+    O.block_sparse_attention(qf[:1], kf[:1], vf, nb, inds, w.scale, [(0, 0, i) for i in qb])
+    t_attn = time.perf_counter() - t0
+    kept = int(sum(int(nb[0, 0, i]) for i in qb))
+    desc = (f"oracle mask build for 1 of {w.B * w.h} (batch, head) pairs "
+            f"({t_mask:.2f} s) + oracle attention for {len(qb)} of {w.B * w.h * w.s1} query "
+            f"blocks ({t_attn:.2f} s); value = kept-block FLOPs of the sampled query "
+            f"blocks / (mask time scaled to those blocks + attention time)")
+    # mask time attributed pro rata to the sampled query blocks
+    secs = t_attn + t_mask * len(qb) / w.s1
+    return attn_flops(w, kept), secs, desc, t_mask, t_attn
+
+
+def run_reference(args, w, thr):
+    """The reference arm: the fp64 oracle as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import nabla_oracle as O
+
+    data = W.generate(w, seed=0)
+    sta = O.sta_mask(*w.grid, *w.sta_half_widths)
+    n_q = 2
+    for _ in range(args.warmup):
+        oracle_sample(w, data, sta, thr, n_qblocks=n_q)
+    flops, secs = 0.0, 0.0
+    desc = ""
+    for s in range(args.steps):
+        f, t, desc, _, _ = oracle_sample(w, data, sta, thr, n_qblocks=n_q, seed=s + 1)
+        flops += f
+        secs += t
+    value = flops / secs / 1e12
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "h": w.h, "D": w.D, "S": w.S, "thr": thr,
+                   "sta_half_widths": list(w.sta_half_widths), "grid": list(w.grid),
+                   "l2": "host run"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, thr):
+    import torch
+
+    rank, world, local, dist = dist_setup(args.gpus)
+    from block_sparse_attention_nablat_gb300 import nabla
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    nabla.load()
+    data = W.generate(w, seed=rank)
+    q, k, v = (nabla.from_storage(data[n], dev) for n in "qkv")
+    sta = nabla.nabla_sta_mask(*w.grid, *w.sta_half_widths, device=dev)
+    kv_nb = torch.empty((w.B, w.h, w.s1), dtype=torch.int32, device=dev)
+    kv_inds = torch.empty((w.B, w.h, w.s1, w.s1), dtype=torch.int32, device=dev)
+    ws = torch.empty(nabla.nabla_build_mask_workspace_bytes(w.B, w.S, w.h, w.D),
+                     dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        nabla.nabla_build_mask(q, k, sta, thr, kv_nb, kv_inds, ws)
+        nabla.nabla_attn_fwd(q, k, v, kv_nb, kv_inds, w.scale, o)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert nabla.nabla_get_last_device_status() == 0
+    kept = int(kv_nb.sum().item())
+
+    # timed region: K steps, events around each kernel group on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(dev)) as clocks:
+        start.record(stream)
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            nabla.nabla_build_mask(q, k, sta, thr, kv_nb, kv_inds, ws)
+            ev[s][1].record(stream)
+            nabla.nabla_attn_fwd(q, k, v, kv_nb, kv_inds, w.scale, o)
+            ev[s][2].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    mask_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    assert nabla.nabla_get_last_device_status() == 0
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    kept_t = torch.tensor([float(kept)], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dist.all_reduce(kept_t, op=dist.ReduceOp.SUM)
+    total_ms = t.item()
+    kept_all = kept_t.item()
+    ms_per_step = total_ms / args.steps
+    value = attn_flops(w, kept_all) / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host q/k/v in, o out, every step
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (torch.empty(q.shape, dtype=q.dtype, pin_memory=True) for _ in range(3))
+        hq.copy_(q), hk.copy_(k), hv.copy_(v)
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            nb2, inds2 = nabla.nabla_build_mask(dq, dk, sta, thr, kv_nb, kv_inds, ws)
+            out = nabla.nabla_attn_fwd(dq, dk, dv, nb2, inds2, w.scale, o)
+            ho.copy_(out, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], dtype=torch.float64,
+                              device=dev)
+        if dist is not None:
+            dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+        nbytes = q.numel() * q.element_size()
+        e2e = {"value": attn_flops(w, kept_all) / (e2e_ms.item() * 1e-3) / 1e12,
+               "unit": "TFLOP/s", "ms_per_step": e2e_ms.item(),
+               "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    peaks, src = load_peaks()
+    attn_tflops = attn_flops(w, kept) / (attn_ms * 1e-3) / 1e12
+    peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    mask_gbs = mask_bytes(w, kept) / (mask_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        from oracle import nabla_oracle as O
+
+        nb_h, inds_h = kv_nb.cpu().numpy(), kv_inds.cpu().numpy()
+        sta_h = sta.cpu().numpy()
+        f, secs, desc, _, _ = oracle_sample(w, data, sta_h, thr, nb_h, inds_h,
+                                            n_qblocks=args.cpu_qblocks)
+        cpu = {"value": f / secs / 1e12, "unit": "TFLOP/s", "cores": host_cores(),
+               "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "h": w.h, "D": w.D, "S": w.S, "thr": thr,
+                   "grid": list(w.grid), "sta_half_widths": list(w.sta_half_widths),
+                   "density": kept / (w.B * w.h * w.s1 * w.s1),
+                   "l2": "inputs larger than L2 (q, k, v %.0f MB each), no flush" % (
+                       q.numel() * q.element_size() / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "parts": {"mask_build_us": mask_ms * 1e3, "mask_build_gbs": mask_gbs,
+                  "attn_ms": attn_ms, "attn_tflops_kept": attn_tflops,
+                  "attn_tflops_dense_equiv": dense_flops(w) / (attn_ms * 1e-3) / 1e12},
+        "roofline": {"bound": "tensor", "kernel": "attention forward", "achieved": attn_tflops,
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": attn_tflops / peak_t,
+                     "traffic": None, "peak_source": f"{src} bf16 sustained"},
+        "mask_roofline": {"bound": "hbm", "kernel": "mask build (pool + map + select)",
+                          "achieved": mask_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                          "frac": mask_gbs / peaks["hbm_gbs"], "frac_of_8000": mask_gbs / 8000.0,
+                          "traffic": None, "peak_source": f"{src} hbm"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * 4,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="720p_bf16", choices=list(W.WORKLOADS))
+    ap.add_argument("--thr", type=float, default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-qblocks", type=int, default=8)
+    args = ap.parse_args()
+    w = W.WORKLOADS[args.workload]
+    thr = args.thr if args.thr is not None else w.thr[0]
+    if args.impl == "reference":
+        run_reference(args, w, thr)
+    else:
+        run_ours(args, w, thr)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,147 @@
+// C ABI of the NABLA hot path: argument checks, workspace layout, dispatch.
+// The operations and their sources are documented in include/nabla.h.
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace nabla {
+
+cudaError_t launch_attn_tc(const void *q, const void *k, const void *v, const Shape &s,
+                           const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *o,
+                           int *status, cudaStream_t st);
+
+namespace {
+
+constexpr int kMaxBlocks = 2048;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool valid_shape(int B, int S, int h, int D) {
+  if (B < 1 || h < 1 || S < 64 || S % 64 != 0) return false;
+  if (D != 64 && D != 128) return false;
+  if (S / 64 > kMaxBlocks) return false;
+  // element counts must fit the kernels' index arithmetic
+  const double elems = (double)B * S * h * D;
+  if (elems > 4.0e12) return false;
+  if ((double)B * h * (S / 64) > 2.0e9) return false;
+  return true;
+}
+
+bool valid_dtype(nabla_dtype dt) { return dt == NABLA_F32 || dt == NABLA_BF16; }
+
+nabla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NABLA_OK : NABLA_ERR_CUDA; }
+
+}  // namespace
+
+MaskWorkspace mask_workspace_layout(const Shape &s) {
+  MaskWorkspace w{};
+  const size_t means = (size_t)s.B * s.h * s.s1 * s.D * sizeof(float);
+  const size_t logits = (size_t)s.B * s.h * s.s1 * s.s1 * sizeof(float);
+  w.qa = 0;
+  w.ka = round_up(w.qa + means, 256);
+  w.logits = round_up(w.ka + means, 256);
+  w.total = round_up(w.logits + logits, 256);
+  return w;
+}
+
+}  // namespace nabla
+
+using nabla::Shape;
+
+extern "C" {
+
+int nabla_abi_version(void) { return 1; }
+
+const char *nabla_status_string(nabla_status s) {
+  switch (s) {
+    case NABLA_OK: return "NABLA_OK";
+    case NABLA_ERR_INVALID_ARG: return "NABLA_ERR_INVALID_ARG";
+    case NABLA_ERR_UNSUPPORTED: return "NABLA_ERR_UNSUPPORTED";
+    case NABLA_ERR_CUDA: return "NABLA_ERR_CUDA";
+    case NABLA_ERR_TIMEOUT: return "NABLA_ERR_TIMEOUT";
+    case NABLA_ERR_BAD_INDEX: return "NABLA_ERR_BAD_INDEX";
+  }
+  return "NABLA_ERR_UNKNOWN";
+}
+
+size_t nabla_build_mask_workspace_bytes(int B, int S, int h, int D) {
+  if (!nabla::valid_shape(B, S, h, D)) return 0;
+  return nabla::mask_workspace_layout(Shape{B, S, h, D, S / 64}).total;
+}
+
+nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int B, int S, int h,
+                              int D, const uint8_t *sta, double thr, int32_t *kv_nb,
+                              int32_t *kv_inds, void *workspace, size_t ws_bytes,
+                              nabla_stream_t stream) {
+  using namespace nabla;
+  if (!valid_shape(B, S, h, D) || !valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
+  if (!(thr > 0.0 && thr <= 1.0)) return NABLA_ERR_INVALID_ARG;  // also rejects NaN
+  if (!q || !k || !sta || !kv_nb || !kv_inds || !workspace) return NABLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(workspace, 256) || !aligned(kv_nb, 4) ||
+      !aligned(kv_inds, 4))
+    return NABLA_ERR_INVALID_ARG;
+  const Shape s{B, S, h, D, S / 64};
+  const MaskWorkspace w = mask_workspace_layout(s);
+  if (ws_bytes < w.total) return NABLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  float *qa = reinterpret_cast<float *>(ws + w.qa);
+  float *ka = reinterpret_cast<float *>(ws + w.ka);
+  float *L = reinterpret_cast<float *>(ws + w.logits);
+  const float t = (float)(1.0 - thr);  // cut level, formed in fp64 then rounded once
+  cudaError_t e = launch_pool(q, k, dt, s, qa, ka, st);
+  if (e == cudaSuccess) e = launch_pooled_map(qa, ka, s, L, st);
+  if (e == cudaSuccess) e = launch_select(L, s, sta, t, kv_nb, kv_inds, st);
+  return from_cuda(e);
+}
+
+nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_dtype dt, int B,
+                            int S, int h, int D, const int32_t *kv_nb, const int32_t *kv_inds,
+                            float scale, void *o, nabla_stream_t stream) {
+  using namespace nabla;
+  if (!valid_shape(B, S, h, D) || !valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return NABLA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !kv_nb || !kv_inds) return NABLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(kv_nb, 4) || !aligned(kv_inds, 4))
+    return NABLA_ERR_INVALID_ARG;
+  const Shape s{B, S, h, D, S / 64};
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  int *status = device_status_ptr(&e);
+  if (!status) return NABLA_ERR_CUDA;
+  if (dt == NABLA_BF16)
+    e = launch_attn_tc(q, k, v, s, kv_nb, kv_inds, scale, o, status, st);
+  else
+    e = launch_attn_simt(q, k, v, dt, s, kv_nb, kv_inds, scale, o, status, st);
+  return from_cuda(e);
+}
+
+nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
+                            nabla_stream_t stream) {
+  if (T < 1 || H < 1 || W < 1 || wt < 0 || wh < 0 || ww < 0 || !sta) return NABLA_ERR_INVALID_ARG;
+  if ((long)T * H * W > nabla::kMaxBlocks) return NABLA_ERR_INVALID_ARG;
+  return nabla::from_cuda(
+      nabla::launch_sta(T, H, W, wt, wh, ww, sta, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nabla_status nabla_get_last_device_status(nabla_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return NABLA_ERR_CUDA;
+  int *status = nabla::device_status_ptr(&e);
+  if (!status) return NABLA_ERR_CUDA;
+  int host = 0;
+  e = cudaMemcpy(&host, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return NABLA_ERR_CUDA;
+  if (host != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return NABLA_ERR_CUDA;
+  }
+  return static_cast<nabla_status>(host);
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Internal launch interface between the C ABI (api.cpp) and the kernels.
+// Not installed; the public contract is include/nabla.h.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "nabla.h"
+
+namespace nabla {
+
+struct Shape {
+  int B, S, h, D, s1;
+};
+
+// Device status codes written by kernels (first writer wins); values match nabla_status.
+enum : int { kDevOk = 0, kDevTimeout = NABLA_ERR_TIMEOUT, kDevBadIndex = NABLA_ERR_BAD_INDEX };
+
+// Address of the library's device status word on the current device (cached per device).
+int *device_status_ptr(cudaError_t *err);
+
+// Byte offsets of the mask-builder workspace regions (each 256-byte aligned).
+struct MaskWorkspace {
+  size_t qa, ka, logits, total;
+};
+MaskWorkspace mask_workspace_layout(const Shape &s);
+
+// K1: block means of q and k -> qa, ka fp32 [B, h, s1, D].
+cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
+                        float *ka, cudaStream_t st);
+// K2a: pooled map L = qa ka^T / sqrt(D), fp32 [B, h, s1, s1].
+cudaError_t launch_pooled_map(const float *qa, const float *ka, const Shape &s, float *L,
+                              cudaStream_t st);
+// K2b: row softmax, ascending running-sum cut at t = 1 - thr, STA OR, CSR emit.
+cudaError_t launch_select(const float *L, const Shape &s, const uint8_t *sta, float t,
+                          int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st);
+// K4: STA window.
+cudaError_t launch_sta(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
+                       cudaStream_t st);
+// K3f: CUDA-core block-sparse attention (fp32 storage).
+cudaError_t launch_attn_simt(const void *q, const void *k, const void *v, nabla_dtype dt,
+                             const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,
+                             float scale, void *o, int *status, cudaStream_t st);
+
+}  // namespace nabla

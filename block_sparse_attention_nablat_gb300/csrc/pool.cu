@@ -1,0 +1,127 @@
+// K1 -- fused block mean-pool of q and k.
+//
+// FastVideo API reference, page "nabla", nablaT_v2 "Map estimation": q and k
+// are viewed head-major as [B, h, S/64, 64, D] and averaged over the 64 tokens
+// of each block; gist.science NABLA summary, Methodology "Downsampling".
+//
+// Reads q, k in their stored [B, S, h, D] layout (no transpose copy): one CTA
+// covers one 64-token block and 64 consecutive 16-byte chunks of the h*D row
+// (1 KB of every token row), so every warp load is 512 contiguous bytes. Four
+// row groups of 64 threads each sum 16 rows with all 16 loads in flight, then
+// the four partial sums are combined in shared memory and written as fp32
+// qa/ka [B, h, s1, D].  HBM-bound: the algorithmic traffic is the single read
+// of q and k plus the (small) fp32 means.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace nabla {
+namespace {
+
+constexpr int kChunksPerCta = 64;
+constexpr int kRowGroups = 4;
+constexpr int kRowsPerThread = 64 / kRowGroups;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <typename T>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+  static constexpr int kElems = 4;
+  __device__ static void add(float *acc, const uint4 &u) {
+    acc[0] += __uint_as_float(u.x);
+    acc[1] += __uint_as_float(u.y);
+    acc[2] += __uint_as_float(u.z);
+    acc[3] += __uint_as_float(u.w);
+  }
+};
+
+template <>
+struct Chunk<__nv_bfloat16> {
+  static constexpr int kElems = 8;
+  __device__ static void add(float *acc, const uint4 &u) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc[2 * e] += __uint_as_float(w[e] << 16);            // low half = even element
+      acc[2 * e + 1] += __uint_as_float(w[e] & 0xffff0000u);  // high half = odd element
+    }
+  }
+};
+
+// grid: (s1, ceil(C / 64), 2 * B); C = h*D / elems-per-chunk.  z selects (b, q|k).
+template <typename T>
+__global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
+                                                   const T *__restrict__ k, int S, int h, int D,
+                                                   float *__restrict__ qa,
+                                                   float *__restrict__ ka) {
+  constexpr int E = Chunk<T>::kElems;
+  __shared__ float part[kRowGroups][kChunksPerCta * E];
+
+  const int i = blockIdx.x;
+  const int b = blockIdx.z >> 1;
+  const bool is_k = blockIdx.z & 1;
+  const int s1 = S >> 6;
+  const int C = h * D / E;
+  const int cx = threadIdx.x % kChunksPerCta;
+  const int rg = threadIdx.x / kChunksPerCta;
+  const int c = blockIdx.y * kChunksPerCta + cx;
+
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+
+  if (c < C) {
+    const T *src = is_k ? k : q;
+    const uint4 *base =
+        reinterpret_cast<const uint4 *>(src + ((size_t)b * S + (size_t)i * 64) * h * D) + c;
+    uint4 v[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r)
+      v[r] = ld_stream(base + (size_t)(rg + kRowGroups * r) * C);
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) Chunk<T>::add(acc, v[r]);
+  }
+#pragma unroll
+  for (int e = 0; e < E; ++e) part[rg][cx * E + e] = acc[e];
+  __syncthreads();
+
+  // 64 chunks * E elements per CTA, spread over the 256 threads.
+  float *dst = is_k ? ka : qa;
+  const int row_elems = h * D;
+  for (int e = threadIdx.x; e < kChunksPerCta * E; e += blockDim.x) {
+    const int col = blockIdx.y * kChunksPerCta * E + e;
+    if (col >= row_elems) break;
+    float s = part[0][e] + part[1][e] + part[2][e] + part[3][e];
+    const int hh = col / D, d = col - hh * D;
+    dst[(((size_t)b * h + hh) * s1 + i) * D + d] = s * (1.0f / 64.0f);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
+                        float *ka, cudaStream_t st) {
+  const int E = dt == NABLA_BF16 ? 8 : 4;
+  const int C = s.h * s.D / E;
+  dim3 grid(s.s1, (C + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
+  if (dt == NABLA_BF16)
+    pool_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), s.S, s.h,
+        s.D, qa, ka);
+  else
+    pool_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(q),
+                                             static_cast<const float *>(k), s.S, s.h, s.D, qa,
+                                             ka);
+  return cudaGetLastError();
+}
+
+}  // namespace nabla

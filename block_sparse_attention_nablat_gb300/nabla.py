@@ -1,0 +1,171 @@
+"""Thin ctypes binding of the C ABI in include/nabla.h (libnabla.so).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  torch supplies device memory (outputs and the mask-builder
+workspace are allocated here with torch when the caller passes none) and the
+current CUDA stream.  If the library is missing, every call raises; there is
+no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnabla.so")
+
+NABLA_OK = 0
+NABLA_F32, NABLA_BF16 = 0, 1
+
+_lib = None
+
+
+class NablaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {nabla_status_string(status)} ({status})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libnabla.so (built by __graft_entry__.build()); raise if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() first")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.nabla_abi_version.restype = i32
+    lib.nabla_abi_version.argtypes = []
+    lib.nabla_status_string.restype = ctypes.c_char_p
+    lib.nabla_status_string.argtypes = [i32]
+    lib.nabla_build_mask_workspace_bytes.restype = sz
+    lib.nabla_build_mask_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.nabla_build_mask.restype = i32
+    lib.nabla_build_mask.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, ctypes.c_double, vp,
+                                     vp, vp, sz, vp]
+    lib.nabla_attn_fwd.restype = i32
+    lib.nabla_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, ctypes.c_float,
+                                   vp, vp]
+    lib.nabla_sta_mask.restype = i32
+    lib.nabla_sta_mask.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.nabla_get_last_device_status.restype = i32
+    lib.nabla_get_last_device_status.argtypes = [vp]
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NABLA_BF16
+    if t.dtype == torch.float32:
+        return NABLA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(status: int, where: str) -> None:
+    if status != NABLA_OK:
+        raise NablaError(status, where)
+
+
+def _shape(q: torch.Tensor) -> Tuple[int, int, int, int]:
+    if q.dim() != 4:
+        raise ValueError("q/k/v must be [B, S, h, D]")
+    if not q.is_contiguous():
+        raise ValueError("q/k/v must be contiguous [B, S, h, D]")
+    return tuple(q.shape)
+
+
+def nabla_abi_version() -> int:
+    return load().nabla_abi_version()
+
+
+def nabla_status_string(status: int) -> str:
+    return load().nabla_status_string(int(status)).decode()
+
+
+def nabla_build_mask_workspace_bytes(B: int, S: int, h: int, D: int) -> int:
+    return load().nabla_build_mask_workspace_bytes(B, S, h, D)
+
+
+def nabla_build_mask(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor, thr: float,
+                     kv_nb: Optional[torch.Tensor] = None,
+                     kv_inds: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None):
+    """(q, k [B,S,h,D], sta [s1,s1] uint8, thr) -> (kv_nb [B,h,s1], kv_inds [B,h,s1,s1]) int32."""
+    lib = load()
+    B, S, h, D = _shape(q)
+    if k.shape != q.shape or k.dtype != q.dtype:
+        raise ValueError("k must match q")
+    s1 = S // 64
+    dev = q.device
+    if kv_nb is None:
+        kv_nb = torch.empty((B, h, s1), dtype=torch.int32, device=dev)
+    if kv_inds is None:
+        kv_inds = torch.empty((B, h, s1, s1), dtype=torch.int32, device=dev)
+    need = lib.nabla_build_mask_workspace_bytes(B, S, h, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.nabla_build_mask(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
+                              float(thr), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nabla_build_mask")
+    return kv_nb, kv_inds
+
+
+def nabla_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb: torch.Tensor,
+                   kv_inds: torch.Tensor, scale: Optional[float] = None,
+                   o: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Block-sparse attention over the kept 64x64 blocks; returns o [B,S,h,D]."""
+    lib = load()
+    B, S, h, D = _shape(q)
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k, v must match q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    st = lib.nabla_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D, _ptr(kv_nb),
+                            _ptr(kv_inds), float(scale), _ptr(o), _stream(stream))
+    _check(st, "nabla_attn_fwd")
+    return o
+
+
+def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """STA window [s1, s1] uint8 on the (T, H, W) block grid."""
+    lib = load()
+    s1 = T * H * W
+    if out is None:
+        out = torch.empty((s1, s1), dtype=torch.uint8, device=device or "cuda")
+    _check(lib.nabla_sta_mask(T, H, W, wt, wh, ww, _ptr(out), _stream(stream)),
+           "nabla_sta_mask")
+    return out
+
+
+def nabla_get_last_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return load().nabla_get_last_device_status(_stream(stream))
+
+
+def from_storage(a: np.ndarray, device) -> torch.Tensor:
+    """numpy storage array (float32, or uint16 bf16 bit patterns) -> device tensor."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)

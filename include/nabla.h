@@ -1,0 +1,159 @@
+/*
+ * nabla.h -- C ABI of the GB300 (sm_103a) NABLA hot path.
+ *
+ * NABLA (Neighborhood-Adaptive Block-Level Attention) builds a data-dependent
+ * 64x64 block mask from mean-pooled queries and keys and then runs softmax
+ * attention over the kept blocks only.  Sources restated here:
+ *   [P1] FastVideo API reference, page "nabla": nablaT_v2 ("Map estimation",
+ *        "Map binarization", BlockMask creation), NablaAttentionImpl.forward,
+ *        NablaAttentionMetadata.
+ *   [P4] gist.science technical summary of "NABLA: Neighborhood Adaptive
+ *        Block-Level Attention", Methodology.
+ *
+ * Conventions shared by every entry point:
+ *   - q, k, v, o are dense, C-contiguous [B, S, h, D] tensors ([P1] forward:
+ *     "q/k/v: [B, S, heads, head_dim]"), element type given by nabla_dtype.
+ *     S must be a multiple of 64 and S/64 (= s1, the number of blocks) at most
+ *     2048; D is 64 or 128.
+ *   - Every pointer argument is DEVICE memory owned by the caller.  q, k, v, o
+ *     must be 16-byte aligned, the workspace 256-byte aligned, kv_nb and kv_inds
+ *     4-byte aligned; sta has no alignment rule.  The library allocates no device memory
+ *     and keeps no state between calls other than a per-kernel device status
+ *     word (see nabla_get_last_device_status).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) of the CURRENT device.  A returned NABLA_OK means
+ *     the arguments were valid and the kernels were launched.
+ *   - Errors are returned, never raised on the device: invalid arguments are
+ *     rejected on the host before anything is launched; launch failures give
+ *     NABLA_ERR_CUDA; device-side conditions (a bounded wait that gave up, an
+ *     out-of-range block index) are recorded in a device status word and
+ *     reported by nabla_get_last_device_status.
+ *   - Causal masking is not offered ([P1] NablaAttentionImpl rejects causal).
+ *     There is no sequence-parallel entry point: the mask spans the whole
+ *     sequence ([P1] module description).
+ */
+#ifndef NABLA_H
+#define NABLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st *nabla_stream_t;
+
+typedef enum {
+  NABLA_OK = 0,
+  NABLA_ERR_INVALID_ARG = 1, /* bad shape, dtype, threshold, pointer or size */
+  NABLA_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. no sm_103 device) */
+  NABLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+  NABLA_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
+  NABLA_ERR_BAD_INDEX = 5    /* kv_nb / kv_inds held an out-of-range entry (skipped) */
+} nabla_status;
+
+typedef enum {
+  NABLA_F32 = 0, /* float32 storage, float32 arithmetic */
+  NABLA_BF16 = 1 /* bfloat16 storage, float32 accumulation */
+} nabla_dtype;
+
+/* Version of this ABI (bumped on any signature change). */
+int nabla_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *nabla_status_string(nabla_status s);
+
+/*
+ * Scratch bytes nabla_build_mask needs for a shape: the fp32 block means of q
+ * and k ([B, h, s1, D] each) and the fp32 pooled map ([B, h, s1, s1]), each
+ * region 256-byte aligned.  Returns 0 for an invalid shape.
+ */
+size_t nabla_build_mask_workspace_bytes(int B, int S, int h, int D);
+
+/*
+ * nabla_build_mask -- the nablaT_v2 mask builder ([P1] nablaT_v2; [P4]
+ * Downsampling, Reduced Attention, CDF Thresholding, Hybrid Integration).
+ *
+ * For every (b, h, query block i):
+ *   qa_i = mean of the 64 query tokens of block i, ka_j likewise for keys;
+ *   p_i  = softmax_j( <qa_i, ka_j> / sqrt(D) );
+ *   sort p_i ascending (ties: lower block index first), running sum c;
+ *   block j is kept iff c(j) >= 1 - thr, or sta[i*s1 + j] != 0;
+ *   kv_nb[(b*h + hh)*s1 + i]           = number of kept blocks,
+ *   kv_inds[((b*h + hh)*s1 + i)*s1 + n] = n-th kept block, ascending, n < kv_nb.
+ * Entries of a kv_inds row at positions >= kv_nb are left unwritten.
+ *
+ *   q, k       [B, S, h, D] device, element type dt.
+ *   sta        [s1, s1] device uint8, 0/1, shared by every batch and head
+ *              ([P1] NablaAttentionMetadata: a block-level [1,1,S/64,S/64] window).
+ *   thr        kept-mass threshold, 0 < thr <= 1 (thr = 1 keeps every block).
+ *   kv_nb      [B, h, s1] device int32, written.
+ *   kv_inds    [B, h, s1, s1] device int32, written (kept prefix of each row).
+ *   workspace  device scratch of ws_bytes >= nabla_build_mask_workspace_bytes().
+ * Arithmetic is fp32 (means accumulated in fp32 from the stored values); the
+ * result can differ from an exact evaluation only for blocks whose running
+ * sum lies within float32 rounding of 1 - thr.
+ * Errors: NABLA_ERR_INVALID_ARG for S % 64 != 0, s1 > 2048, D not in {64,128},
+ * B or h < 1, thr outside (0, 1], NULL or misaligned pointers, short workspace.
+ */
+nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int B, int S,
+                              int h, int D, const uint8_t *sta, double thr, int32_t *kv_nb,
+                              int32_t *kv_inds, void *workspace, size_t ws_bytes,
+                              nabla_stream_t stream);
+
+/*
+ * nabla_attn_fwd -- block-sparse attention forward over the kept 64x64 blocks
+ * ([P1] NablaAttentionImpl.forward: flex_attention with a BlockMask of full
+ * 64x64 blocks, non-causal; [P4] Expansion).
+ *
+ * For every (b, hh, query token s in block i), with J the tokens of the blocks
+ * kv_inds[b, hh, i, 0 .. kv_nb[b, hh, i]-1]:
+ *   o[b, s, hh, :] = sum_{u in J} softmax_u( scale * <q_s, k_u> ) v_u,
+ * computed with an online softmax in fp32; o = 0 for a row with kv_nb = 0.
+ * bf16: QK^T and PV run on the tcgen05 tensor cores (bf16 operands, fp32
+ * accumulators; P is rounded to bf16 before PV); o is written as bf16.
+ * f32: fp32 CUDA-core arithmetic throughout; o is written as fp32.
+ *
+ *   q, k, v, o  [B, S, h, D] device, element type dt; o is overwritten.
+ *   kv_nb       [B, h, s1] device int32, each in [0, s1].
+ *   kv_inds     [B, h, s1, s1] device int32; the first kv_nb entries of each row
+ *               are block indices in [0, s1), strictly ascending.
+ *   scale       softmax scale (normally 1/sqrt(D), flex_attention's default).
+ * Out-of-range kv_nb / kv_inds entries are skipped and reported as
+ * NABLA_ERR_BAD_INDEX by nabla_get_last_device_status; they never cause an
+ * out-of-bounds access.
+ * Errors: NABLA_ERR_INVALID_ARG as for nabla_build_mask (shape, dtype,
+ * pointers) and for a non-finite scale.
+ */
+nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_dtype dt, int B,
+                            int S, int h, int D, const int32_t *kv_nb, const int32_t *kv_inds,
+                            float scale, void *o, nabla_stream_t stream);
+
+/*
+ * nabla_sta_mask -- the spatio-temporal window ([P1] NablaAttentionMetadata
+ * "sta_mask"; [P4] Hybrid Integration with STA).  The pages do not show its
+ * construction; this library's reading: on the (T, H, W) block grid with
+ * block index (t*H + y)*W + x, sta[i*s1 + j] = 1 iff |t_i - t_j| <= wt,
+ * |y_i - y_j| <= wh and |x_i - x_j| <= ww (no wrap-around), else 0.
+ *   sta   [s1, s1] device uint8 with s1 = T*H*W <= 2048, written.
+ * Errors: NABLA_ERR_INVALID_ARG for T, H, W < 1, s1 > 2048, negative half
+ * widths, NULL sta.
+ */
+nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
+                            nabla_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status words that
+ * the kernels above set (bounded-wait timeouts, skipped out-of-range indices).
+ * Returns NABLA_OK when nothing was recorded, NABLA_ERR_CUDA when the
+ * synchronisation itself failed, else the first recorded condition.
+ */
+nabla_status nabla_get_last_device_status(nabla_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NABLA_H */
