@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T *__restrict__ q,
 
   for (int n = 0; n < nb; ++n) {
     const int j = list[n];
-    if (j < 0 || j >= s1) {  // uniform over the CTA
+    if (j < 0 || j >= s1 || (n > 0 && list[n - 1] >= j)) {  // uniform over the CTA
       if (tid == 0) atomicCAS(status, kDevOk, kDevBadIndex);
       continue;
     }

@@ -180,6 +180,23 @@ def ambiguous_blocks(c: np.ndarray, t: float, sta: Optional[np.ndarray] = None,
     return amb
 
 
+def near_tie_blocks(p: np.ndarray, cdf_mask: np.ndarray, sta: Optional[np.ndarray] = None,
+                    rel: float = 1e-5) -> np.ndarray:
+    """Blocks in a near-tie that straddles the cut (reading of the tolerance):
+    a dropped block j and a kept block k of the same row whose probabilities
+    differ by at most rel * max(p_j, p_k).  Their ascending order cannot be
+    resolved in float32, and swapping them moves each running sum by a whole
+    block mass, so either decision is admissible for both.  STA blocks excluded."""
+    dropped = ~cdf_mask
+    big = np.where(dropped, p, -np.inf).max(axis=-1, keepdims=True)  # heaviest dropped
+    small = np.where(cdf_mask, p, np.inf).min(axis=-1, keepdims=True)  # lightest kept
+    near = big >= small * (1.0 - rel)
+    out = near & ((dropped & (p >= small * (1.0 - rel))) | (cdf_mask & (p * (1.0 - rel) <= big)))
+    if sta is not None:
+        out &= ~np.asarray(sta, dtype=bool)[None, None]
+    return out
+
+
 # ---------------------------------------------------------------------------
 # a7: block-sparse attention.  [P1] NablaAttentionImpl.forward: flex_attention
 # with the block mask (64x64 blocks, all full blocks, default scale, non-causal).
