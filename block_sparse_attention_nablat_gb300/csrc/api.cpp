@@ -128,6 +128,10 @@ nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t
       nabla::launch_sta(T, H, W, wt, wh, ww, sta, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nabla_status nabla_selftest_bounded_wait(nabla_stream_t stream) {
+  return nabla::from_cuda(nabla::launch_bounded_wait_probe(reinterpret_cast<cudaStream_t>(stream)));
+}
+
 nabla_status nabla_get_last_device_status(nabla_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return NABLA_ERR_CUDA;

@@ -16,6 +16,9 @@ struct Shape {
 // Device status codes written by kernels (first writer wins); values match nabla_status.
 enum : int { kDevOk = 0, kDevTimeout = NABLA_ERR_TIMEOUT, kDevBadIndex = NABLA_ERR_BAD_INDEX };
 
+// Diagnostic: a wait nothing satisfies must end as a recorded timeout.
+cudaError_t launch_bounded_wait_probe(cudaStream_t st);
+
 // Address of the library's device status word on the current device (cached per device).
 int *device_status_ptr(cudaError_t *err);
 

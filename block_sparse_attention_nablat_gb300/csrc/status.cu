@@ -1,9 +1,23 @@
 // The library's device status word: kernels record a bounded wait that gave up
 // or an out-of-range block index here (first writer wins) instead of trapping.
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace {
 __device__ int g_status;
+
+// One CTA waits on an mbarrier that nothing arrives on, through the same
+// bounded wait the attention kernel uses; it must give up and record a timeout.
+__global__ void bounded_wait_probe(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    nabla::tc::mbar_init(&bar, 1);
+    nabla::tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    nabla::tc::mbar_wait(&bar, 0, nullptr, &g_status, nabla::kDevTimeout, limit_ns);
+}
 
 constexpr int kMaxDevices = 64;
 int *g_status_addr[kMaxDevices];
@@ -26,6 +40,11 @@ int *device_status_ptr(cudaError_t *err) {
     g_status_addr[dev] = static_cast<int *>(p);
   }
   return g_status_addr[dev];
+}
+
+cudaError_t launch_bounded_wait_probe(cudaStream_t st) {
+  bounded_wait_probe<<<1, 32, 0, st>>>(20000000ull);  // 20 ms
+  return cudaGetLastError();
 }
 
 }  // namespace nabla

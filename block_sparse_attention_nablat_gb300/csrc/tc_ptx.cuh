@@ -51,14 +51,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: every legitimate wait here is microseconds
 
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          int *status, int code) {
+                                          int *status, int code, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0u) {
       if (abort && *abort) return false;
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         atomicCAS(status, 0, code);
         if (abort) *abort = 1;
         return false;

@@ -54,6 +54,8 @@ def load() -> ctypes.CDLL:
                                    vp, vp]
     lib.nabla_sta_mask.restype = i32
     lib.nabla_sta_mask.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp]
+    lib.nabla_selftest_bounded_wait.restype = i32
+    lib.nabla_selftest_bounded_wait.argtypes = [vp]
     lib.nabla_get_last_device_status.restype = i32
     lib.nabla_get_last_device_status.argtypes = [vp]
     _lib = lib
@@ -156,6 +158,11 @@ def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=Non
     _check(lib.nabla_sta_mask(T, H, W, wt, wh, ww, _ptr(out), _stream(stream)),
            "nabla_sta_mask")
     return out
+
+
+def nabla_selftest_bounded_wait(stream=None) -> None:
+    """Enqueue the bounded-wait probe (it must end as a recorded timeout)."""
+    _check(load().nabla_selftest_bounded_wait(_stream(stream)), "nabla_selftest_bounded_wait")
 
 
 def nabla_get_last_device_status(stream=None) -> int:

@@ -145,6 +145,15 @@ nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t
                             nabla_stream_t stream);
 
 /*
+ * Diagnostic of the failure-detection path (no counterpart on the pages):
+ * enqueues one CTA that waits on an mbarrier nothing ever arrives on, through
+ * the same bounded wait the attention kernel uses, with a 20 ms limit.  The
+ * wait gives up and records NABLA_ERR_TIMEOUT in the device status word; the
+ * context stays usable.  Returns NABLA_OK when the probe was launched.
+ */
+nabla_status nabla_selftest_bounded_wait(nabla_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status words that
  * the kernels above set (bounded-wait timeouts, skipped out-of-range indices).
  * Returns NABLA_OK when nothing was recorded, NABLA_ERR_CUDA when the

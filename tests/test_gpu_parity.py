@@ -10,6 +10,7 @@ Tolerances (fixed by the benchmark spec, not by the pages):
         mean-abs 1e-3 (bf16).
 """
 import math
+import time
 
 import numpy as np
 import pytest
@@ -266,8 +267,14 @@ def test_out_of_range_index_is_reported_not_faulted(nabla):
     inds[..., 1] = 1
     inds[0, 0, 2, 1] = 4  # out of range: must be skipped and reported
     nb[0, 0, 3] = 5       # count beyond s1
-    o = nabla.nabla_attn_fwd(*[nabla.from_storage(data[n], DEV) for n in "qkv"],
-                             torch.from_numpy(nb).to(DEV), torch.from_numpy(inds).to(DEV))
+    args = [nabla.from_storage(data[n], DEV) for n in "qkv"]
+    nbt, indst = torch.from_numpy(nb).to(DEV), torch.from_numpy(inds).to(DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    o = nabla.nabla_attn_fwd(*args, nbt, indst)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert elapsed < 0.5, f"{elapsed:.2f} s: a bounded wait expired"
     assert nabla.nabla_get_last_device_status() == 5
     assert nabla.nabla_get_last_device_status() == 0  # cleared
     assert torch.isfinite(o.float()).all()
@@ -282,3 +289,16 @@ def test_mask_builder_deterministic(nabla):
     nb = a[0]
     for idx in np.ndindex(nb.shape):
         assert np.array_equal(a[1][idx][:nb[idx]], b[1][idx][:nb[idx]])
+
+
+def test_bounded_wait_gives_up_and_reports_timeout(nabla):
+    """A device wait that nothing satisfies ends after its limit with
+    NABLA_ERR_TIMEOUT recorded, and the context stays usable."""
+    assert nabla.nabla_get_last_device_status() == 0
+    t0 = time.perf_counter()
+    nabla.nabla_selftest_bounded_wait()
+    assert nabla.nabla_get_last_device_status() == 4
+    assert time.perf_counter() - t0 < 5.0
+    assert nabla.nabla_get_last_device_status() == 0
+    x = torch.ones(1024, device=DEV)
+    assert float(x.sum().item()) == 1024.0
