@@ -49,6 +49,9 @@ def load() -> ctypes.CDLL:
     lib.nabla_build_mask.restype = i32
     lib.nabla_build_mask.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, ctypes.c_double, vp,
                                      vp, vp, sz, vp]
+    lib.nabla_build_mask_noalloc.restype = i32
+    lib.nabla_build_mask_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, ctypes.c_double,
+                                             vp, vp, vp]
     lib.nabla_attn_fwd.restype = i32
     lib.nabla_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, ctypes.c_float,
                                    vp, vp]
@@ -127,6 +130,17 @@ def nabla_build_mask(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor, thr: f
                               float(thr), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nabla_build_mask")
+    return kv_nb, kv_inds
+
+
+def nabla_build_mask_noalloc(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor, thr: float,
+                             kv_nb: torch.Tensor, kv_inds: torch.Tensor, stream=None):
+    """nabla_build_mask without a workspace: the library's fixed device scratch is
+    used instead (see include/nabla.h); outputs must be preallocated by the caller."""
+    B, S, h, D = _shape(q)
+    st = load().nabla_build_mask_noalloc(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
+                                         float(thr), _ptr(kv_nb), _ptr(kv_inds), _stream(stream))
+    _check(st, "nabla_build_mask_noalloc")
     return kv_nb, kv_inds
 
 

@@ -104,6 +104,39 @@ nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int 
                               nabla_stream_t stream);
 
 /*
+ * nabla_build_mask_noalloc -- nabla_build_mask for callers that cannot
+ * allocate device memory.  The NABLA pages have no counterpart; this entry
+ * point is a property of this library only.
+ *
+ * Some callers cannot call cudaMalloc: an engine that reserves all device
+ * memory for its own pool at start-up and forbids allocation afterwards, a
+ * latency-critical loop that cannot afford the device-wide synchronisation
+ * cudaMalloc and cudaFree may imply, or a plug-in running inside a host
+ * program whose memory budget it does not control.  This variant needs no
+ * workspace argument: its scratch (the fp32 block means and pooled map) is a
+ * NABLA_NOALLOC_SCRATCH_BYTES array the library defines in device memory.
+ * Every GPU that loads the library holds that array until the process exits.
+ *
+ * Arguments, result and errors are those of nabla_build_mask, minus the
+ * workspace, and the result is identical, plus:
+ *   - shapes whose nabla_build_mask_workspace_bytes() exceeds
+ *     NABLA_NOALLOC_SCRATCH_BYTES are rejected with NABLA_ERR_UNSUPPORTED
+ *     before anything is launched;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture;
+ *   - all calls share the one array, which keeps the last call's contents;
+ *     the kernels overwrite every scratch element they read, so nothing needs
+ *     clearing, but calls whose kernels overlap on the GPU (different streams,
+ *     or unordered host threads) race on it and must be serialised;
+ *   - it calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define NABLA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+nabla_status nabla_build_mask_noalloc(const void *q, const void *k, nabla_dtype dt, int B, int S,
+                                      int h, int D, const uint8_t *sta, double thr,
+                                      int32_t *kv_nb, int32_t *kv_inds, nabla_stream_t stream);
+
+/*
  * nabla_attn_fwd -- block-sparse attention forward over the kept 64x64 blocks
  * ([P1] NablaAttentionImpl.forward: flex_attention with a BlockMask of full
  * 64x64 blocks, non-causal; [P4] Expansion).
