@@ -10,32 +10,36 @@
 //    the M = 128 shape of a single-CTA tcgen05 MMA.  The unit walks the UNION
 //    of the two blocks' kept-KV lists in ascending order; each entry carries
 //    two membership bits, and rows of a block that did not keep an entry get
-//    P = 0 for it (their softmax skips it).  Persistent CTAs (one per SM, the
-//    kernel needs ~225 KB of shared memory and 384 TMEM columns) take units
-//    round-robin in head-major order so concurrently running CTAs share one
-//    head's K/V in L2.
+//    P = 0 for it.  Persistent CTAs (one per SM) take units round-robin in
+//    head-major order, so co-running CTAs share one head's K/V in L2.
+//  * A step covers two KV entries (128 keys).  On this hardware a tcgen05 MMA
+//    costs about 32 + N/2 cycles whatever its N, so S = Q K^T is issued with
+//    N = 128 (both entries of the step in one MMA, from a K "pair slot" whose
+//    rows 64..127 follow rows 0..63) and PV with N = D.
+//  * TMEM: O (128 x D fp32) in columns [0, 128) and three 128-column score
+//    buffers.  With three buffers, QK^T of step s+2 only has to wait for the PV
+//    of step s-1, which is already queued ahead of PV(s), so the tensor pipe
+//    never drains between steps.
 //  * Warp roles: warp 0 builds the unit's entry bitmaps from kv_inds and issues
-//    TMA loads (Q once per unit; K and V tiles of each kept block into a
-//    6-deep ring); warp 1 (one thread) issues all MMAs; warps 4-7 (thread r =
-//    TMEM lane r = query row r) run the online softmax and the epilogue.
-//  * Per step (two KV entries): S = Q K^T as two 128x64 MMAs (K = D) into a
-//    TMEM score buffer (two buffers, so QK of step s+1 overlaps the softmax of
-//    step s); the softmax writes P back over the scores as packed bf16, and
-//    PV accumulates O (128 x D fp32 in TMEM) with P taken straight from TMEM
-//    as the A operand and V (MN-major) from shared memory.
-//  * Online softmax in base 2 with the scale folded in; the running max is
-//    only raised (and O, l rescaled) when it grows by more than 2^8, so the
-//    O correction through TMEM is rare; the result is exact either way since
-//    O and l always share the same reference max.
+//    TMA loads (Q once per unit; K pair slots one step ahead of the per-entry
+//    V tiles); warp 1 (one thread) issues all MMAs; warps 4-7 and 8-11 are two
+//    softmax groups splitting each step's columns (group x takes entry x).
+//    Thread r of a group = TMEM lane r = query row r; the two threads of a row
+//    exchange their partial row max through shared memory every step (a
+//    barrier per warp pair), so both use one reference max and one O.
+//  * Online softmax in base 2 with the scale folded in (packed f32x2 FMA for
+//    the exponent argument); the running max is raised (and O, l rescaled)
+//    only when it grows by more than 2^8, so the O correction through TMEM is
+//    rare; the result is exact either way since O and l share the max.
 //  * Every mbarrier wait is bounded (1 s); on expiry the kernel records
-//    NABLA_ERR_TIMEOUT, all roles stop, and TMEM is released.  Out-of-range or
-//    unsorted kv_inds entries and out-of-range kv_nb are skipped and recorded
-//    as NABLA_ERR_BAD_INDEX.
+//    NABLA_ERR_TIMEOUT, all roles stop waiting (the warp-pair barriers are
+//    still met in lockstep, so no partner is left behind), in-flight MMAs and
+//    copies are drained and TMEM is released.  Out-of-range or unsorted
+//    kv_inds entries and out-of-range kv_nb are skipped and recorded as
+//    NABLA_ERR_BAD_INDEX.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
-
-#include <cstring>
 
 #include "internal.h"
 #include "tc_ptx.cuh"
@@ -56,29 +60,54 @@ struct UnitInfo {
 
 template <int D>
 struct Cfg {
-  static constexpr int kBoxes = D / 64;             // 64-column (128-byte) swizzle boxes
-  static constexpr int kQBytes = 128 * D * 2;       // two query blocks
-  static constexpr int kTileBytes = 64 * D * 2;     // one K or V block
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = D == 128 ? 6 : 12;
-  static constexpr uint32_t kOCol = 0;              // O accumulator: TMEM columns [0, D)
-  static constexpr uint32_t kSCol = 128;            // score buffers: [128, 256) and [256, 384)
+  static constexpr int kBoxes = D / 64;          // 64-column (128-byte) swizzle boxes
+  static constexpr int kQBytes = 128 * D * 2;    // two query blocks
+  static constexpr int kTileBytes = 64 * D * 2;  // one K or V block
+  static constexpr int kPairBox = 128 * 128;     // one 64-column box of a K pair slot (128 rows)
+  static constexpr int kPairBytes = 2 * kTileBytes;
+  static constexpr int kKStages = 3;             // K pair slots (steps)
+  static constexpr int kVStages = D == 128 ? 4 : 8;  // V tiles (entries)
+  static constexpr int kSBufs = 3;
+  static constexpr uint32_t kSCol = 128;         // score buffer b at TMEM columns 128 + 128 b
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kIdescQK = idesc_bf16(128, 64, 0, 0);
+  static constexpr uint32_t kIdescQK2 = idesc_bf16(128, 128, 0, 0);
+  static constexpr uint32_t kIdescQK1 = idesc_bf16(128, 64, 0, 0);
   static constexpr uint32_t kIdescPV = idesc_bf16(128, D, 0, 1);
+  static constexpr int kThreads = 384;
   // shared-memory layout (offsets from a 1024-byte aligned base)
   static constexpr int kOffQ = 0;
-  static constexpr int kOffStages = kQBytes;
-  static constexpr int kOffInfo = kOffStages + kStages * kStageBytes;
-  static constexpr int kOffBars = kOffInfo + 2 * (int)sizeof(UnitInfo);
-  static constexpr int kNumBars = 2 * kStages + 14;
-  static constexpr int kOffMisc = kOffBars + 8 * kNumBars;
-  static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kPairBytes;
+  static constexpr int kOffInfo = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffXmax = kOffInfo + 2 * (int)sizeof(UnitInfo);  // [2 parity][2 grp][128]
+  static constexpr int kOffXl = kOffXmax + 2 * 2 * 128 * 4;             // [2 grp][128]
+  static constexpr int kOffBars = kOffXl + 2 * 128 * 4;
 };
 
+// All mbarriers and small shared flags, laid out by the compiler (8-byte aligned).
+template <int NK, int NV, int NS>
+struct SharedSync {
+  uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+  uint64_t q_full, q_empty, info_full[2], info_empty[2];
+  uint64_t s_full[NS], p_full[NS], pv_done[NS];
+  uint64_t o_free, drain;
+  uint32_t tmem_slot;
+  int abort;
+};
+
+template <int D>
+using SyncOf = SharedSync<Cfg<D>::kKStages, Cfg<D>::kVStages, Cfg<D>::kSBufs>;
+
+template <int D>
+constexpr int smem_bytes() {
+  return 1024 + Cfg<D>::kOffBars + (int)sizeof(SyncOf<D>);
+}
+static_assert(smem_bytes<128>() <= 232448, "shared memory budget (D=128)");
+static_assert(smem_bytes<64>() <= 232448, "shared memory budget (D=64)");
+
 struct Bars {
-  uint64_t *kv_full, *kv_empty, *q_full, *q_empty, *info_full, *info_empty, *s_full, *p_full,
-      *pv_done, *o_free, *drain;
+  uint64_t *k_full, *k_empty, *v_full, *v_empty, *q_full, *q_empty, *info_full, *info_empty,
+      *s_full, *p_full, *pv_done, *o_free, *drain;
 };
 
 struct Cursor {
@@ -105,20 +134,91 @@ struct Params {
   int *status;
 };
 
+struct Unit {
+  int b, hh, pr;
+};
+__device__ __forceinline__ Unit decode(long u, int npairs, int h) {
+  const long bh = u / npairs;
+  Unit r;
+  r.pr = (int)(u - bh * npairs);
+  r.b = (int)(bh / h);
+  r.hh = (int)(bh - (long)r.b * h);
+  return r;
+}
+
+// packed fp32 pairs (sm_100+ f32x2 arithmetic)
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ void pair_sync(int q4) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + q4) : "memory");
+}
+
+// P for 32 scores: 2^(s * scale_log2 - m) in fp32 (row-sum accumulators updated),
+// packed to bf16 pairs and stored over 16 TMEM columns at taddr.
+__device__ __forceinline__ void exp_pack_store(const uint32_t (&r)[32], uint64_t sc2, uint64_t nm2,
+                                               uint64_t &acc0, uint64_t &acc1, uint32_t taddr) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    float x0, x1, y0, y1;
+    unf2(fma2(f2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), sc2, nm2), x0, x1);
+    unf2(fma2(f2(__uint_as_float(r[2 * i + 2]), __uint_as_float(r[2 * i + 3])), sc2, nm2), y0,
+         y1);
+    x0 = ex2(x0);
+    x1 = ex2(x1);
+    y0 = ex2(y0);
+    y1 = ex2(y1);
+    acc0 = add2(acc0, f2(x0, x1));
+    acc1 = add2(acc1, f2(y0, y1));
+    pk[i] = pack_bf16x2(x0, x1);
+    pk[i + 1] = pack_bf16x2(y0, y1);
+  }
+  tmem_st16(taddr, pk);
+}
+
 // On the abort path: wait (bounded, ignoring the abort flag) until the last
 // copies this thread issued have landed, so none writes shared memory after exit.
 template <int D>
-__device__ void drain_copies(const Params &P, const Bars &bar, uint32_t ge, uint32_t kq,
-                             bool q_loaded) {
+__device__ void drain_copies(const Params &P, const Bars &bar, uint32_t gk, uint32_t ge,
+                             uint32_t kq) {
   using C = Cfg<D>;
-  const uint32_t first = ge > (uint32_t)C::kStages ? ge - C::kStages : 0u;
-  for (uint32_t e = first; e < ge; ++e)
-    mbar_wait(&bar.kv_full[e % C::kStages], (e / C::kStages) & 1u, nullptr, P.status,
+  for (uint32_t e = gk > (uint32_t)C::kKStages ? gk - C::kKStages : 0u; e < gk; ++e)
+    mbar_wait(&bar.k_full[e % C::kKStages], (e / C::kKStages) & 1u, nullptr, P.status,
               kDevTimeout);
-  if (q_loaded && kq > 0) mbar_wait(bar.q_full, (kq - 1) & 1u, nullptr, P.status, kDevTimeout);
+  for (uint32_t e = ge > (uint32_t)C::kVStages ? ge - C::kVStages : 0u; e < ge; ++e)
+    mbar_wait(&bar.v_full[e % C::kVStages], (e / C::kVStages) & 1u, nullptr, P.status,
+              kDevTimeout);
+  if (kq > 0) mbar_wait(bar.q_full, (kq - 1) & 1u, nullptr, P.status, kDevTimeout);
 }
 
-// Warp 0: entry bitmaps + TMA loads.
+// Warp 0: entry bitmaps + TMA loads (Q per unit; K pair slots one step ahead of V).
 template <int D>
 __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                          const CUtensorMap *tmV, uint8_t *smem, UnitInfo *info, const Bars &bar,
@@ -127,19 +227,20 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
   const int lane = threadIdx.x & 31;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1, words = (s1 + 31) >> 5;
   const long units = (long)P.B * P.h * npairs;
-  uint32_t ge = 0, kq = 0;
+  uint32_t gk = 0, ge = 0, kq = 0;  // K pair slots issued, V tiles issued, Q tiles issued
+  bool stop = false;  // lane 0: a wait gave up; every lane leaves together at the loop top
   int k = 0;
   for (long u = blockIdx.x; u < units; u += gridDim.x, ++k) {
     __syncwarp();
-    if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+    if (__shfl_sync(0xffffffffu, (stop || *abort) ? 1 : 0, 0)) break;
     const int ub = k & 1;
     UnitInfo &inf = info[ub];
     bool ok = true;
-    if (lane == 0) ok = mbar_wait(&bar.info_empty[ub], ((k >> 1) & 1) ^ 1, abort, P.status, kDevTimeout);
-    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-    const long bh = u / npairs;
-    const int pr = (int)(u - bh * npairs);
-    const int b = (int)(bh / P.h), hh = (int)(bh - (long)b * P.h);
+    if (lane == 0)
+      ok = mbar_wait(&bar.info_empty[ub], ((k >> 1) & 1) ^ 1, abort, P.status, kDevTimeout);
+    if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+    const Unit un = decode(u, npairs, P.h);
+    const long bh = (long)un.b * P.h + un.hh;
     // ---- union of the two kept lists as bitmaps
     for (int w = lane; w < kMaxWords; w += 32) {
       inf.a[w] = 0u;
@@ -149,7 +250,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     bool bad = false;
 #pragma unroll
     for (int side = 0; side < 2; ++side) {
-      const int qb = 2 * pr + side;
+      const int qb = 2 * un.pr + side;
       if (qb >= s1) break;
       const size_t row = (size_t)bh * s1 + qb;
       int cnt = P.kv_nb[row];
@@ -178,41 +279,63 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     if (lane == 0) inf.n = cnt;
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.info_full[ub]);
-    // ---- TMA loads (one thread)
-    if (lane == 0 && cnt > 0) {
-      bool go = mbar_wait(bar.q_empty, (kq & 1) ^ 1, abort, P.status, kDevTimeout);
-      if (go) {
-        mbar_expect_tx(bar.q_full, C::kQBytes);
+    if (lane != 0 || cnt == 0) continue;
+    // ---- TMA loads (one thread; on failure it sets `stop` and rejoins the warp)
+    if (!mbar_wait(bar.q_empty, (kq & 1) ^ 1, abort, P.status, kDevTimeout)) {
+      stop = true;
+      continue;
+    }
+    mbar_expect_tx(bar.q_full, C::kQBytes);
+#pragma unroll
+    for (int c = 0; c < C::kBoxes; ++c)
+      tma_load_4d(smem + C::kOffQ + c * 128 * 128, tmQ, bar.q_full, c * 64, un.hh, un.pr * 128,
+                  un.b);
+    ++kq;
+    const int steps = (cnt + 1) >> 1;
+    Cursor ck{0, inf.a[0] | inf.b[0]}, cv = ck;
+    bool go = true;
+    auto load_k = [&](int s) {  // both entries of step s into one pair slot
+      const uint32_t ks = gk % C::kKStages;
+      go = go && mbar_wait(&bar.k_empty[ks], ((gk / C::kKStages) & 1) ^ 1, abort, P.status,
+                           kDevTimeout);
+      if (!go) return;
+      const int ne = (2 * s + 1 < cnt) ? 2 : 1;
+      mbar_expect_tx(&bar.k_full[ks], ne * C::kTileBytes);
+      uint8_t *slot = smem + C::kOffK + ks * C::kPairBytes;
+      for (int x = 0; x < ne; ++x) {
+        uint32_t fl;
+        const int j = next_entry(inf, ck, fl);
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_4d(smem + C::kOffQ + c * 128 * 128, tmQ, bar.q_full, c * 64, hh, pr * 128, b);
+          tma_load_4d(slot + c * C::kPairBox + x * 64 * 128, tmK, &bar.k_full[ks], c * 64, un.hh,
+                      j * 64, un.b);
       }
-      ++kq;
-      Cursor cur{0, inf.a[0] | inf.b[0]};
-      for (int e = 0; go && e < cnt; ++e, ++ge) {
-        if (*abort) {
-          go = false;
-          break;
-        }
-        uint32_t fl;
-        const int j = next_entry(inf, cur, fl);
-        const uint32_t st = ge % C::kStages, rnd = ge / C::kStages;
-        if (!mbar_wait(&bar.kv_empty[st], (rnd & 1) ^ 1, abort, P.status, kDevTimeout)) {
-          go = false;
-          break;
-        }
-        uint8_t *kt = smem + C::kOffStages + st * C::kStageBytes;
-        uint8_t *vt = kt + C::kTileBytes;
-        mbar_expect_tx(&bar.kv_full[st], C::kStageBytes);
+      ++gk;
+    };
+    auto load_v = [&]() {  // next entry's V tile
+      const uint32_t vs = ge % C::kVStages;
+      go = go && mbar_wait(&bar.v_empty[vs], ((ge / C::kVStages) & 1) ^ 1, abort, P.status,
+                           kDevTimeout);
+      if (!go) return;
+      uint32_t fl;
+      const int j = next_entry(inf, cv, fl);
+      mbar_expect_tx(&bar.v_full[vs], C::kTileBytes);
 #pragma unroll
-        for (int c = 0; c < C::kBoxes; ++c) {
-          tma_load_4d(kt + c * 64 * 128, tmK, &bar.kv_full[st], c * 64, hh, j * 64, b);
-          tma_load_4d(vt + c * 64 * 128, tmV, &bar.kv_full[st], c * 64, hh, j * 64, b);
-        }
-      }
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_4d(smem + C::kOffV + vs * C::kTileBytes + c * 64 * 128, tmV, &bar.v_full[vs],
+                    c * 64, un.hh, j * 64, un.b);
+      ++ge;
+    };
+    load_k(0);
+    for (int s = 0; s < steps && go; ++s) {
+      if (s + 1 < steps) load_k(s + 1);
+      load_v();
+      if (2 * s + 1 < cnt) load_v();
+      if (*abort) go = false;
     }
+    if (!go) stop = true;
   }
-  if (lane == 0 && *abort) drain_copies<D>(P, bar, ge, kq, true);
+  if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, ge, kq);
 }
 
 // Warp 1, lane 0: MMA issue.
@@ -222,11 +345,16 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
   using C = Cfg<D>;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
-  const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-  const uint32_t st_addr = smem_u32(smem + C::kOffStages);
-  uint32_t ge = 0, gs = 0, kq = 0;
+  // Matrix descriptors are built once; an operand step only advances the start
+  // address field (bits 0-13, address >> 4), which cannot carry for addresses
+  // below 256 KB, so each MMA issues with one 64-bit add of an immediate.
+  const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+  const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+  const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + C::kOffV), 64 * 128, 1024);
+  uint32_t gk = 0, ge = 0, gs = 0, kq = 0;
   int k = 0;
-  for (long u = blockIdx.x; u < units && !*abort; u += gridDim.x, ++k) {
+  bool ok = true;
+  for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
     const int ub = k & 1;
     if (!mbar_wait(&bar.info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) break;
     const int n = info[ub].n;
@@ -234,62 +362,61 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
     if (steps > 0) {
       if (!mbar_wait(bar.q_full, kq & 1, abort, P.status, kDevTimeout)) break;
       tc_fence_after();
-      bool ok = true;
       auto issue_qk = [&](int s) {
-        const uint32_t g = gs + s, sb = g & 1u;
-        ok = ok && mbar_wait(&bar.pv_done[sb], ((g >> 1) & 1u) ^ 1u, abort, P.status, kDevTimeout);
-        for (int x = 0; x < 2 && ok; ++x) {
-          const int e = 2 * s + x;
-          if (e >= n) break;
-          const uint32_t ee = ge + e, st = ee % C::kStages;
-          ok = mbar_wait(&bar.kv_full[st], (ee / C::kStages) & 1u, abort, P.status, kDevTimeout);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t d = tmem + C::kSCol + sb * 128 + x * 64;
-          const uint32_t kb = st_addr + st * C::kStageBytes;
+        const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
+        // score buffer b was last read by the PV of step g-3
+        ok = ok && mbar_wait(&bar.pv_done[b], (use & 1u) ^ 1u, abort, P.status, kDevTimeout);
+        const uint32_t kk_slot = (gk + s) % C::kKStages, krnd = (gk + s) / C::kKStages;
+        ok = ok && mbar_wait(&bar.k_full[kk_slot], krnd & 1u, abort, P.status, kDevTimeout);
+        if (!ok) return;
+        tc_fence_after();
+        const uint32_t d = tmem + C::kSCol + b * 128;
+        const uint64_t kd = k_desc + (uint64_t)((kk_slot * C::kPairBytes) >> 4);
+        const uint32_t idesc = (2 * s + 1 < n) ? C::kIdescQK2 : C::kIdescQK1;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (uint32_t)(kk & 3) * 32u;  // 16-element step inside the 128-B atom
-            const uint64_t a = smem_desc_sw128(q_addr + (kk >> 2) * 128 * 128 + koff, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kb + (kk >> 2) * 64 * 128 + koff, 16, 1024);
-            mma_ss(d, a, bd, C::kIdescQK, kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          // 16-element k-step: 32 B inside a 128-B swizzle atom; every 4 steps the next
+          // 64-column box (16 KB of Q, one 128-row box of the K pair slot)
+          const uint64_t a = q_desc + (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::kPairBox) + (kk & 3) * 32) >> 4);
+          mma_ss(d, a, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        if (ok) mma_commit(&bar.s_full[sb]);
+        mma_commit(&bar.k_empty[kk_slot]);  // K pair slot reusable once this QK^T is done
+        mma_commit(&bar.s_full[b]);
       };
       issue_qk(0);
-      if (steps == 1 && ok) mma_commit(bar.q_empty);
+      if (steps > 1) issue_qk(1);
+      if (ok && steps <= 2) mma_commit(bar.q_empty);
       for (int s = 0; s < steps && ok; ++s) {
-        if (s + 1 < steps) {
-          issue_qk(s + 1);
-          if (s + 2 == steps && ok) mma_commit(bar.q_empty);  // last QK of the unit issued
-        }
-        if (!ok) break;
-        const uint32_t g = gs + s, sb = g & 1u;
+        const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
         if (s == 0 && kq > 0) {
           ok = mbar_wait(bar.o_free, (kq - 1) & 1u, abort, P.status, kDevTimeout);
           if (!ok) break;
         }
-        ok = mbar_wait(&bar.p_full[sb], (g >> 1) & 1u, abort, P.status, kDevTimeout);
+        ok = mbar_wait(&bar.p_full[b], use & 1u, abort, P.status, kDevTimeout);
         if (!ok) break;
         tc_fence_after();
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < 2 && ok; ++x) {
           const int e = 2 * s + x;
           if (e >= n) break;
-          const uint32_t st = (ge + e) % C::kStages;
-          const uint32_t vb = st_addr + st * C::kStageBytes + C::kTileBytes;
+          const uint32_t ee = ge + e, vs = ee % C::kVStages;
+          ok = mbar_wait(&bar.v_full[vs], (ee / C::kVStages) & 1u, abort, P.status, kDevTimeout);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = v_desc + (uint64_t)((vs * C::kTileBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t a = tmem + C::kSCol + sb * 128 + x * 32 + kk * 8;
-            const uint64_t bd = smem_desc_sw128(vb + kk * 16 * 128, 64 * 128, 1024);
-            mma_ts(tmem + C::kOCol, a, bd, C::kIdescPV, (s > 0 || x > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t a = tmem + C::kSCol + b * 128 + x * 64 + kk * 8;
+            const uint64_t bd = vd + (uint64_t)((kk * 16 * 128) >> 4);  // next 16 KV rows
+            mma_ts(tmem, a, bd, C::kIdescPV, (s > 0 || x > 0 || kk > 0) ? 1u : 0u);
           }
+          mma_commit(&bar.v_empty[vs]);
         }
-        mma_commit(&bar.pv_done[sb]);
-        for (int x = 0; x < 2; ++x) {
-          const int e = 2 * s + x;
-          if (e >= n) break;
-          mma_commit(&bar.kv_empty[(ge + e) % C::kStages]);
+        if (!ok) break;
+        mma_commit(&bar.pv_done[b]);
+        if (s + 2 < steps) {
+          issue_qk(s + 2);  // waits for PV(s-1) only: PV(s) is already queued behind it
+          if (ok && s + 3 == steps) mma_commit(bar.q_empty);  // last QK of the unit issued
         }
       }
       if (!ok) break;
@@ -297,6 +424,7 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
     }
     mbar_arrive(&bar.info_empty[ub]);
     ge += n;
+    gk += steps;
     gs += steps;
   }
   // never release TMEM / exit with MMAs in flight (matters only on the abort path)
@@ -304,200 +432,195 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
   mbar_wait(bar.drain, 0, nullptr, P.status, kDevTimeout);
 }
 
-// Warps 4-7: online softmax + epilogue.  Thread = TMEM lane = query row.
+// Warps 4-11: two softmax groups splitting each step's columns + the epilogue.
 template <int D>
-__device__ void softmax_epilogue(const Params &P, UnitInfo *info, const Bars &bar, uint32_t tmem,
-                                 volatile int *abort) {
+__device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem, const Bars &bar,
+                                 uint32_t tmem, volatile int *abort) {
   using C = Cfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q4 = warp & 3;
+  const int grp = (warp - 4) >> 2;  // takes entry grp of every step; owns O columns grp*D/2..
+  const int q4 = warp & 3;          // TMEM lane quadrant; partner warp = same q4, other group
   const int row = q4 * 32 + lane;
   const int half = row >> 6;
   const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+  float *xmax = reinterpret_cast<float *>(smem + C::kOffXmax);
+  float *xl = reinterpret_cast<float *>(smem + C::kOffXl);
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   const float sl2 = P.scale_log2;
+  const bool pos_scale = sl2 >= 0.f;
   uint32_t gs = 0;
   int k = 0;
-  for (long u = blockIdx.x; u < units && !*abort; u += gridDim.x, ++k) {
+  bool live = true;  // false after a wait gave up: keep meeting the pair barriers, do no work
+  for (long u = blockIdx.x; u < units; u += gridDim.x, ++k) {
     const int ub = k & 1;
-    if (!mbar_wait(&bar.info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) break;
-    const UnitInfo &inf = info[ub];
-    const int n = inf.n;
+    live = __all_sync(0xffffffffu, live && mbar_wait(&bar.info_full[ub], (k >> 1) & 1, abort,
+                                                      P.status, kDevTimeout));
+    // both threads of a row must run the same number of pair barriers: agree on `live`
+    // (and so on n) through the pair exchange slot
+    xl[grp * 128 + row] = live ? 1.f : 0.f;
+    pair_sync(q4);
+    live = __all_sync(0xffffffffu, live && xl[(grp ^ 1) * 128 + row] != 0.f);
+    pair_sync(q4);
+    const int n = live ? info[ub].n : 0;
     const int steps = (n + 1) >> 1;
-    const long bh = u / npairs;
-    const int pr = (int)(u - bh * npairs);
-    const int b = (int)(bh / P.h), hh = (int)(bh - (long)b * P.h);
-    const int qb = 2 * pr + half;
+    const Unit un = decode(u, npairs, P.h);
+    const int qb = 2 * un.pr + half;
     float m_run = -INFINITY, l_run = 0.f;
-    Cursor cur{0, inf.a[0] | inf.b[0]};
-    bool ok = true;
+    Cursor cur{0, info[ub].a[0] | info[ub].b[0]};
     for (int s = 0; s < steps; ++s) {
-      const uint32_t g = gs + s, sb = g & 1u;
+      const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
       uint32_t f0 = 0, f1 = 0;
-      next_entry(inf, cur, f0);
+      next_entry(info[ub], cur, f0);
       const bool has1 = 2 * s + 1 < n;
-      if (has1) next_entry(inf, cur, f1);
-      const bool act0 = (f0 >> half) & 1u;
-      const bool act1 = has1 && ((f1 >> half) & 1u);
-      ok = mbar_wait(&bar.s_full[sb], (g >> 1) & 1u, abort, P.status, kDevTimeout);
-      if (!ok) break;
+      if (has1) next_entry(info[ub], cur, f1);
+      const bool mine = grp == 0 || has1;
+      const bool act = mine && ((((grp ? f1 : f0) >> half) & 1u) != 0u);
+      live = __all_sync(0xffffffffu, live && mbar_wait(&bar.s_full[b], use & 1u, abort, P.status,
+                                                        kDevTimeout));
       tc_fence_after();
-      const uint32_t sbase = tmem + lane_base + C::kSCol + sb * 128;
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      if (act0) {
-        tmem_ld32(sbase + 0, r0);
+      const uint32_t sbase = tmem + lane_base + C::kSCol + b * 128 + grp * 64;
+      uint32_t r0[32], r1[32];
+      float mx = -INFINITY;
+      if (live && act) {
+        tmem_ld32(sbase, r0);
         tmem_ld32(sbase + 32, r1);
-      }
-      if (act1) {
-        tmem_ld32(sbase + 64, r2);
-        tmem_ld32(sbase + 96, r3);
-      }
-      tmem_wait_ld();
-      if (act0) {
+        tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
-      }
-      if (act1) {
-        reg_fence(r2);
-        reg_fence(r3);
-      }
-      // row max of the raw scores (the scale may be negative)
-      float hi = -INFINITY, lo = INFINITY;
-      if (act0) {
+        float a0, a1, a2, a3;
+        if (pos_scale) {
+          a0 = a1 = a2 = a3 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x0 = __uint_as_float(r0[i]), x1 = __uint_as_float(r1[i]);
-          hi = fmaxf(hi, fmaxf(x0, x1));
-          lo = fminf(lo, fminf(x0, x1));
-        }
-      }
-      if (act1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x0 = __uint_as_float(r2[i]), x1 = __uint_as_float(r3[i]);
-          hi = fmaxf(hi, fmaxf(x0, x1));
-          lo = fminf(lo, fminf(x0, x1));
-        }
-      }
-      const bool any = act0 || act1;
-      if (any) {
-        const float mx = sl2 >= 0.f ? hi * sl2 : lo * sl2;
-        const float m_new = fmaxf(m_run, mx);
-        const bool resc = m_run != -INFINITY && m_new > m_run + 8.0f;
-        if (__any_sync(0xffffffffu, resc)) {
-          // O must hold every PV up to the previous step before it is rescaled
-          const uint32_t gp = g - 1;
-          ok = mbar_wait(&bar.pv_done[gp & 1u], (gp >> 1) & 1u, abort, P.status, kDevTimeout);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
+          for (int i = 0; i < 32; i += 4) {
+            a0 = max3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+            a1 = max3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+            a2 = max3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+            a3 = max3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
           }
+          a0 = max3(a0, a1, fmaxf(a2, a3));
+        } else {
+          a0 = a1 = a2 = a3 = INFINITY;
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            a0 = min3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+            a1 = min3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+            a2 = min3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+            a3 = min3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+          }
+          a0 = min3(a0, a1, fminf(a2, a3));
+        }
+        mx = a0 * sl2;
+      }
+      // exchange the partial row max with the partner thread (same row, other group)
+      float *xm = xmax + (size_t)(g & 1u) * 2 * 128;
+      xm[grp * 128 + row] = mx;
+      pair_sync(q4);
+      const float m_new = fmaxf(m_run, fmaxf(mx, xm[(grp ^ 1) * 128 + row]));
+      const bool any_row = m_new != -INFINITY;  // some block kept for this row so far
+      const bool resc = m_run != -INFINITY && m_new > m_run + 8.0f;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O must hold every PV up to the previous step before it is rescaled;
+        // each group rescales its half of the D columns (the decision is the same
+        // in both groups, both hold the same m_run)
+        const uint32_t gp = g - 1;
+        const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
+        live = __all_sync(0xffffffffu,
+                          live && mbar_wait(&bar.pv_done[gp % C::kSBufs], (gp / C::kSBufs) & 1u,
+                                            abort, P.status, kDevTimeout));
+        if (live) {
           tc_fence_after();
-          const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t t[32];
-            tmem_ld32(tmem + lane_base + C::kOCol + c * 32, t);
+            const uint32_t ta = tmem + lane_base + grp * (D / 2) + c * 16;
+            uint32_t t[16];
+            tmem_ld16(ta, t);
             tmem_wait_ld();
-            reg_fence(t);
+            reg_fence16(t);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-            tmem_st32(tmem + lane_base + C::kOCol + c * 32, t);
+            for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+            tmem_st16(ta, t);
           }
           tmem_wait_st();
-          if (resc) {
-            l_run *= alpha;
-            m_run = m_new;
-          }
         }
-        if (m_run == -INFINITY) m_run = m_new;
-      }
-      // P = 2^(s * scale * log2 e - m), packed bf16 pairs, over the score columns
-      float lsum = 0.f;
-      uint32_t pk[32];
-      if (act0) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a0 = ex2(fmaf(__uint_as_float(r0[2 * i]), sl2, -m_run));
-          const float a1 = ex2(fmaf(__uint_as_float(r0[2 * i + 1]), sl2, -m_run));
-          const float b0 = ex2(fmaf(__uint_as_float(r1[2 * i]), sl2, -m_run));
-          const float b1 = ex2(fmaf(__uint_as_float(r1[2 * i + 1]), sl2, -m_run));
-          lsum += (a0 + a1) + (b0 + b1);
-          pk[i] = pack_bf16x2(a0, a1);
-          pk[16 + i] = pack_bf16x2(b0, b1);
+        if (resc) {
+          l_run *= alpha;
+          m_run = m_new;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = 0u;
       }
-      tmem_st32(sbase + 0, pk);
-      if (has1) {
-        if (act1) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a0 = ex2(fmaf(__uint_as_float(r2[2 * i]), sl2, -m_run));
-            const float a1 = ex2(fmaf(__uint_as_float(r2[2 * i + 1]), sl2, -m_run));
-            const float b0 = ex2(fmaf(__uint_as_float(r3[2 * i]), sl2, -m_run));
-            const float b1 = ex2(fmaf(__uint_as_float(r3[2 * i + 1]), sl2, -m_run));
-            lsum += (a0 + a1) + (b0 + b1);
-            pk[i] = pack_bf16x2(a0, a1);
-            pk[16 + i] = pack_bf16x2(b0, b1);
-          }
+      if (m_run == -INFINITY && any_row) m_run = m_new;
+      if (live && mine) {
+        if (act) {
+          const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_run, -m_run);
+          uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;
+          exp_pack_store(r0, sc2, nm2, acc0, acc1, sbase);
+          exp_pack_store(r1, sc2, nm2, acc0, acc1, sbase + 16);
+          float s0, s1v, s2, s3;
+          unf2(acc0, s0, s1v);
+          unf2(acc1, s2, s3);
+          l_run += (s0 + s1v) + (s2 + s3);
         } else {
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = 0u;
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          tmem_st16(sbase, pk);
+          tmem_st16(sbase + 16, pk);
         }
-        tmem_st32(sbase + 32, pk);
+        tmem_wait_st();
       }
-      l_run += lsum;
-      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar.p_full[sb]);
+      mbar_arrive(&bar.p_full[b]);
     }
-    if (!ok) break;
-    // ---- epilogue: O / l -> bf16 -> o[b, qb*64 + r, hh, :]
+    // ---- epilogue: O / (l_0 + l_1) -> bf16; each group writes its half of the columns
     if (steps > 0) {
       const uint32_t gl = gs + steps - 1;
-      ok = mbar_wait(&bar.pv_done[gl & 1u], (gl >> 1) & 1u, abort, P.status, kDevTimeout);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      live = __all_sync(0xffffffffu,
+                        live && mbar_wait(&bar.pv_done[gl % C::kSBufs], (gl / C::kSBufs) & 1u,
+                                          abort, P.status, kDevTimeout));
       tc_fence_after();
     }
-    const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+    xl[grp * 128 + row] = live ? l_run : -1.f;  // l >= 0; -1 marks a half that gave up
+    pair_sync(q4);
+    const float l_other = xl[(grp ^ 1) * 128 + row];
+    pair_sync(q4);  // both read before the slot is written again
+    live = __all_sync(0xffffffffu, live && l_other >= 0.f);
+    const float lt = l_run + l_other;
+    const float inv = lt > 0.f ? 1.0f / lt : 0.f;
     const bool row_valid = qb < s1;
     __nv_bfloat16 *orow =
-        P.o + (((size_t)b * P.S + (size_t)qb * 64 + (row & 63)) * P.h + hh) * D;
+        P.o + (((size_t)un.b * P.S + (size_t)qb * 64 + (row & 63)) * P.h + un.hh) * D;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t t[32];
-      if (steps > 0) {
-        tmem_ld32(tmem + lane_base + C::kOCol + c * 32, t);
+    for (int cc = 0; cc < D / 32; ++cc) {
+      const int c = grp * (D / 32) + cc;  // this group's 16-column pieces
+      uint32_t t[16];
+      if (live && steps > 0) {
+        tmem_ld16(tmem + lane_base + c * 16, t);
         tmem_wait_ld();
-        reg_fence(t);
+        reg_fence16(t);
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) t[i] = 0u;
+        for (int i = 0; i < 16; ++i) t[i] = 0u;
       }
-      uint32_t w[16];
+      uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
+      for (int i = 0; i < 8; ++i)
         w[i] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
-      if (row_valid) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+      if (live && row_valid) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
     tc_fence_before();
     if (steps > 0) mbar_arrive(bar.o_free);
     mbar_arrive(&bar.info_empty[ub]);
     gs += steps;
+    if (!live) break;  // both halves of every pair leave at the same unit
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, Params P) {
   using C = Cfg<D>;
@@ -505,38 +628,46 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   UnitInfo *info = reinterpret_cast<UnitInfo *>(smem + C::kOffInfo);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBars);
+  SyncOf<D> *sync = reinterpret_cast<SyncOf<D> *>(smem + C::kOffBars);
   Bars bar;
-  bar.kv_full = bars;
-  bar.kv_empty = bars + C::kStages;
-  bar.q_full = bars + 2 * C::kStages;
-  bar.q_empty = bar.q_full + 1;
-  bar.info_full = bar.q_full + 2;
-  bar.info_empty = bar.q_full + 4;
-  bar.s_full = bar.q_full + 6;
-  bar.p_full = bar.q_full + 8;
-  bar.pv_done = bar.q_full + 10;
-  bar.o_free = bar.q_full + 12;
-  bar.drain = bar.q_full + 13;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
-  volatile int *abort = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+  bar.k_full = sync->k_full;
+  bar.k_empty = sync->k_empty;
+  bar.v_full = sync->v_full;
+  bar.v_empty = sync->v_empty;
+  bar.q_full = &sync->q_full;
+  bar.q_empty = &sync->q_empty;
+  bar.info_full = sync->info_full;
+  bar.info_empty = sync->info_empty;
+  bar.s_full = sync->s_full;
+  bar.p_full = sync->p_full;
+  bar.pv_done = sync->pv_done;
+  bar.o_free = &sync->o_free;
+  bar.drain = &sync->drain;
+  uint32_t *tmem_slot = &sync->tmem_slot;
+  volatile int *abort = &sync->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&bar.kv_full[i], 1);
-      mbar_init(&bar.kv_empty[i], 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      mbar_init(&bar.k_full[i], 1);
+      mbar_init(&bar.k_empty[i], 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
+      mbar_init(&bar.v_full[i], 1);
+      mbar_init(&bar.v_empty[i], 1);
     }
     mbar_init(bar.q_full, 1);
     mbar_init(bar.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.info_full[i], 1);
-      mbar_init(&bar.info_empty[i], 128 + 1);
+      mbar_init(&bar.info_empty[i], 256 + 1);
+    }
+    for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.p_full[i], 128);
+      mbar_init(&bar.p_full[i], 256);
       mbar_init(&bar.pv_done[i], 1);
     }
-    mbar_init(bar.o_free, 128);
+    mbar_init(bar.o_free, 256);
     mbar_init(bar.drain, 1);
     *abort = 0;
     tma_prefetch_desc(&tmQ);
@@ -556,7 +687,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) mma_issuer<D>(P, smem, info, bar, tmem, abort);
     __syncwarp();
   } else if (warp >= 4) {
-    softmax_epilogue<D>(P, info, bar, tmem, abort);
+    softmax_epilogue<D>(P, info, smem, bar, tmem, abort);
   }
 
   tc_fence_before();
@@ -618,13 +749,13 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const Shape &s
     return err;
   auto kern = attn_tc_kernel<D>;
   if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  C::kSmemBytes)) != cudaSuccess)
+                                  smem_bytes<D>())) != cudaSuccess)
     return err;
   const long units = (long)s.B * s.h * ((s.s1 + 1) / 2);
   const int grid = (int)(units < sms ? units : sms);
   Params p{static_cast<__nv_bfloat16 *>(o), kv_nb, kv_inds, s.B, s.S, s.h,
            scale * 1.4426950408889634f, status};
-  kern<<<grid, 256, C::kSmemBytes, st>>>(mq, mk, mv, p);
+  kern<<<grid, C::kThreads, smem_bytes<D>(), st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
