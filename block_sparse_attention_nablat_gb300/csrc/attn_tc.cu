@@ -22,7 +22,9 @@
 //    never drains between steps.
 //  * Warp roles: warp 0 builds the unit's entry bitmaps from kv_inds and issues
 //    TMA loads (Q once per unit; K pair slots one step ahead of the per-entry
-//    V tiles); warp 1 (one thread) issues all MMAs; warps 4-7 and 8-11 are two
+//    V tiles); one thread of warp 1 issues every QK^T and one thread of warp 2
+//    every PV (two issue streams, so one stream's waits never leave the tensor
+//    pipe without queued work); warps 4-7 and 8-11 are two
 //    softmax groups splitting each step's columns (group x takes entry x).
 //    Thread r of a group = TMEM lane r = query row r; the two threads of a row
 //    exchange their partial row max through shared memory every step (a
@@ -338,10 +340,23 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
   if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, ge, kq);
 }
 
-// Warp 1, lane 0: MMA issue.
+// Ring position: slot index and phase parity advanced without division.
+template <int N>
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == (uint32_t)N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Warp 1, lane 0: all QK^T MMAs.  QK^T of step g writes score buffer g % 3 once
+// the PV of step g-3 (the last reader of that buffer) is done.
 template <int D>
-__device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const Bars &bar,
-                           uint32_t tmem, volatile int *abort) {
+__device__ void qk_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const Bars &bar,
+                          uint32_t tmem, volatile int *abort) {
   using C = Cfg<D>;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
@@ -350,8 +365,9 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
   // below 256 KB, so each MMA issues with one 64-bit add of an immediate.
   const uint64_t q_desc = smem_desc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
   const uint64_t k_desc = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-  const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + C::kOffV), 64 * 128, 1024);
-  uint32_t gk = 0, ge = 0, gs = 0, kq = 0;
+  Ring<C::kSBufs> sb;       // score buffer of the next step; phase = its use count parity
+  Ring<C::kKStages> ks;     // K pair slot of the next step
+  uint32_t kq = 0;
   int k = 0;
   bool ok = true;
   for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
@@ -362,16 +378,13 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
     if (steps > 0) {
       if (!mbar_wait(bar.q_full, kq & 1, abort, P.status, kDevTimeout)) break;
       tc_fence_after();
-      auto issue_qk = [&](int s) {
-        const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
-        // score buffer b was last read by the PV of step g-3
-        ok = ok && mbar_wait(&bar.pv_done[b], (use & 1u) ^ 1u, abort, P.status, kDevTimeout);
-        const uint32_t kk_slot = (gk + s) % C::kKStages, krnd = (gk + s) / C::kKStages;
-        ok = ok && mbar_wait(&bar.k_full[kk_slot], krnd & 1u, abort, P.status, kDevTimeout);
-        if (!ok) return;
+      for (int s = 0; s < steps; ++s) {
+        ok = mbar_wait(&bar.pv_done[sb.slot], sb.phase ^ 1u, abort, P.status, kDevTimeout) &&
+             mbar_wait(&bar.k_full[ks.slot], ks.phase, abort, P.status, kDevTimeout);
+        if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tmem + C::kSCol + b * 128;
-        const uint64_t kd = k_desc + (uint64_t)((kk_slot * C::kPairBytes) >> 4);
+        const uint32_t d = tmem + C::kSCol + sb.slot * 128;
+        const uint64_t kd = k_desc + (uint64_t)((ks.slot * C::kPairBytes) >> 4);
         const uint32_t idesc = (2 * s + 1 < n) ? C::kIdescQK2 : C::kIdescQK1;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -381,53 +394,70 @@ __device__ void mma_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const
           const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::kPairBox) + (kk & 3) * 32) >> 4);
           mma_ss(d, a, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar.k_empty[kk_slot]);  // K pair slot reusable once this QK^T is done
-        mma_commit(&bar.s_full[b]);
-      };
-      issue_qk(0);
-      if (steps > 1) issue_qk(1);
-      if (ok && steps <= 2) mma_commit(bar.q_empty);
-      for (int s = 0; s < steps && ok; ++s) {
-        const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
-        if (s == 0 && kq > 0) {
-          ok = mbar_wait(bar.o_free, (kq - 1) & 1u, abort, P.status, kDevTimeout);
-          if (!ok) break;
-        }
-        ok = mbar_wait(&bar.p_full[b], use & 1u, abort, P.status, kDevTimeout);
-        if (!ok) break;
-        tc_fence_after();
-        for (int x = 0; x < 2 && ok; ++x) {
-          const int e = 2 * s + x;
-          if (e >= n) break;
-          const uint32_t ee = ge + e, vs = ee % C::kVStages;
-          ok = mbar_wait(&bar.v_full[vs], (ee / C::kVStages) & 1u, abort, P.status, kDevTimeout);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = v_desc + (uint64_t)((vs * C::kTileBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t a = tmem + C::kSCol + b * 128 + x * 64 + kk * 8;
-            const uint64_t bd = vd + (uint64_t)((kk * 16 * 128) >> 4);  // next 16 KV rows
-            mma_ts(tmem, a, bd, C::kIdescPV, (s > 0 || x > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bar.v_empty[vs]);
-        }
-        if (!ok) break;
-        mma_commit(&bar.pv_done[b]);
-        if (s + 2 < steps) {
-          issue_qk(s + 2);  // waits for PV(s-1) only: PV(s) is already queued behind it
-          if (ok && s + 3 == steps) mma_commit(bar.q_empty);  // last QK of the unit issued
-        }
+        mma_commit(&bar.k_empty[ks.slot]);  // K pair slot reusable once this QK^T is done
+        mma_commit(&bar.s_full[sb.slot]);
+        if (s + 1 == steps) mma_commit(bar.q_empty);  // Q reusable after the unit's last QK^T
+        sb.next();
+        ks.next();
       }
       if (!ok) break;
       ++kq;
     }
     mbar_arrive(&bar.info_empty[ub]);
-    ge += n;
-    gk += steps;
-    gs += steps;
   }
   // never release TMEM / exit with MMAs in flight (matters only on the abort path)
+  mma_commit(bar.drain);
+  mbar_wait(bar.drain, 0, nullptr, P.status, kDevTimeout);
+}
+
+// Warp 2, lane 0: all PV MMAs, O += P V for each entry of a step once both softmax
+// groups have written that step's P.
+template <int D>
+__device__ void pv_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const Bars &bar,
+                          uint32_t tmem, volatile int *abort) {
+  using C = Cfg<D>;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
+  const long units = (long)P.B * P.h * npairs;
+  const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + C::kOffV), 64 * 128, 1024);
+  Ring<C::kSBufs> sb;
+  Ring<C::kVStages> vs;
+  uint32_t kq = 0;
+  int k = 0;
+  bool ok = true;
+  for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
+    const int ub = k & 1;
+    if (!mbar_wait(&bar.info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) break;
+    const int n = info[ub].n;
+    const int steps = (n + 1) >> 1;
+    if (steps > 0) {
+      // O of the previous unit must have been read out before the first PV overwrites it
+      if (kq > 0 && !mbar_wait(bar.o_free, (kq - 1) & 1u, abort, P.status, kDevTimeout)) break;
+      for (int s = 0; s < steps; ++s) {
+        ok = mbar_wait(&bar.p_full[sb.slot], sb.phase, abort, P.status, kDevTimeout);
+        if (!ok) break;
+        tc_fence_after();
+        for (int x = 0; x < 2 && 2 * s + x < n; ++x) {
+          ok = mbar_wait(&bar.v_full[vs.slot], vs.phase, abort, P.status, kDevTimeout);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t vd = v_desc + (uint64_t)((vs.slot * C::kTileBytes) >> 4);
+          const uint32_t a0 = tmem + C::kSCol + sb.slot * 128 + x * 64;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem, a0 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::kIdescPV,
+                   (s > 0 || x > 0 || kk > 0) ? 1u : 0u);  // next 16 KV rows
+          mma_commit(&bar.v_empty[vs.slot]);
+          vs.next();
+        }
+        if (!ok) break;
+        mma_commit(&bar.pv_done[sb.slot]);
+        sb.next();
+      }
+      if (!ok) break;
+      ++kq;
+    }
+    mbar_arrive(&bar.info_empty[ub]);
+  }
   mma_commit(bar.drain);
   mbar_wait(bar.drain, 0, nullptr, P.status, kDevTimeout);
 }
@@ -660,7 +690,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.info_full[i], 1);
-      mbar_init(&bar.info_empty[i], 256 + 1);
+      mbar_init(&bar.info_empty[i], 256 + 2);  // softmax threads + both MMA issuers
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bar.s_full[i], 1);
@@ -668,7 +698,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar.pv_done[i], 1);
     }
     mbar_init(bar.o_free, 256);
-    mbar_init(bar.drain, 1);
+    mbar_init(bar.drain, 2);  // one commit per MMA-issuing thread
     *abort = 0;
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
@@ -684,7 +714,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     producer<D>(P, &tmQ, &tmK, &tmV, smem, info, bar, abort);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<D>(P, smem, info, bar, tmem, abort);
+    if (lane == 0) qk_issuer<D>(P, smem, info, bar, tmem, abort);
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) pv_issuer<D>(P, smem, info, bar, tmem, abort);
     __syncwarp();
   } else if (warp >= 4) {
     softmax_epilogue<D>(P, info, smem, bar, tmem, abort);
