@@ -38,11 +38,13 @@ nabla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NABLA_OK : NAB
 
 MaskWorkspace mask_workspace_layout(const Shape &s) {
   MaskWorkspace w{};
-  const size_t means = (size_t)s.B * s.h * s.s1 * s.D * sizeof(float);
+  w.mean_bytes = round_up((size_t)s.B * s.h * s.s1 * s.D * sizeof(float), 256);
   const size_t logits = (size_t)s.B * s.h * s.s1 * s.s1 * sizeof(float);
-  w.qa = 0;
-  w.ka = round_up(w.qa + means, 256);
-  w.logits = round_up(w.ka + means, 256);
+  w.qa_hi = 0;
+  w.qa_lo = w.mean_bytes;
+  w.ka_hi = 2 * w.mean_bytes;
+  w.ka_lo = 3 * w.mean_bytes;
+  w.logits = 4 * w.mean_bytes;
   w.total = round_up(w.logits + logits, 256);
   return w;
 }
@@ -88,12 +90,17 @@ nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int 
   if (ws_bytes < w.total) return NABLA_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   char *ws = static_cast<char *>(workspace);
-  float *qa = reinterpret_cast<float *>(ws + w.qa);
-  float *ka = reinterpret_cast<float *>(ws + w.ka);
+  float *qa_hi = reinterpret_cast<float *>(ws + w.qa_hi);
+  float *qa_lo = reinterpret_cast<float *>(ws + w.qa_lo);
+  float *ka_hi = reinterpret_cast<float *>(ws + w.ka_hi);
+  float *ka_lo = reinterpret_cast<float *>(ws + w.ka_lo);
   float *L = reinterpret_cast<float *>(ws + w.logits);
   const float t = (float)(1.0 - thr);  // cut level, formed in fp64 then rounded once
-  cudaError_t e = launch_pool(q, k, dt, s, qa, ka, st);
-  if (e == cudaSuccess) e = launch_pooled_map(qa, ka, s, L, st);
+  cudaError_t e;
+  int *status = device_status_ptr(&e);
+  if (!status) return NABLA_ERR_CUDA;
+  e = launch_pool(q, k, dt, s, qa_hi, ka_hi, w.mean_bytes / sizeof(float), st);
+  if (e == cudaSuccess) e = launch_pooled_map(qa_hi, qa_lo, ka_hi, ka_lo, s, L, status, st);
   if (e == cudaSuccess) e = launch_select(L, s, sta, t, kv_nb, kv_inds, st);
   return from_cuda(e);
 }

@@ -733,23 +733,6 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 get_encode(cudaError_t *err) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    *err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                            cudaEnableDefault, &q);
-    if (*err != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
-      if (*err == cudaSuccess) *err = cudaErrorNotSupported;
-      return nullptr;
-    }
-    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  *err = cudaSuccess;
-  return fn;
-}
-
 // [B, S, h, D] bf16 viewed as a 4-D tensor (D, h, S, B); box = 64 columns x `rows` tokens.
 bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *ptr,
               const Shape &s, int rows) {
@@ -770,7 +753,7 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const Shape &s
                      int *status, cudaStream_t st) {
   using C = Cfg<D>;
   cudaError_t err;
-  auto enc = get_encode(&err);
+  auto enc = tensor_map_encoder(&err);
   if (!enc) return err;
   CUtensorMap mq, mk, mv;
   if (!make_map(enc, &mq, q, s, 128) || !make_map(enc, &mk, k, s, 64) ||

@@ -1,6 +1,8 @@
 // Internal launch interface between the C ABI (api.cpp) and the kernels.
 // Not installed; the public contract is include/nabla.h.
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -22,17 +24,24 @@ cudaError_t launch_bounded_wait_probe(cudaStream_t st);
 // Address of the library's device status word on the current device (cached per device).
 int *device_status_ptr(cudaError_t *err);
 
-// Byte offsets of the mask-builder workspace regions (each 256-byte aligned).
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(cudaError_t *err);
+
+// Byte offsets of the mask-builder workspace regions (each 256-byte aligned):
+// block means of q and k as tf32 hi/lo pairs, equally spaced by `mean_bytes`
+// (qa_hi, qa_lo, ka_hi, ka_lo), then the fp32 pooled map.
 struct MaskWorkspace {
-  size_t qa, ka, logits, total;
+  size_t mean_bytes, qa_hi, qa_lo, ka_hi, ka_lo, logits, total;
 };
 MaskWorkspace mask_workspace_layout(const Shape &s);
 
-// K1: block means of q and k -> qa, ka fp32 [B, h, s1, D].
+// K1: block means of q and k -> tf32 hi at qa/ka, tf32 lo at +lo_off elements,
+// each [B, h, s1, D].
 cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
-                        float *ka, cudaStream_t st);
-// K2a: pooled map L = qa ka^T / sqrt(D), fp32 [B, h, s1, s1].
-cudaError_t launch_pooled_map(const float *qa, const float *ka, const Shape &s, float *L,
+                        float *ka, size_t lo_off, cudaStream_t st);
+// K2a: pooled map L = qa ka^T / sqrt(D), fp32 [B, h, s1, s1], on tcgen05 (3-term tf32).
+cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const float *ka_hi,
+                              const float *ka_lo, const Shape &s, float *L, int *status,
                               cudaStream_t st);
 // K2b: row softmax, ascending running-sum cut at t = 1 - thr, STA OR, CSR emit.
 cudaError_t launch_select(const float *L, const Shape &s, const uint8_t *sta, float t,

@@ -8,9 +8,11 @@
 // covers one 64-token block and 64 consecutive 16-byte chunks of the h*D row
 // (1 KB of every token row), so every warp load is 512 contiguous bytes. Four
 // row groups of 64 threads each sum 16 rows with all 16 loads in flight, then
-// the four partial sums are combined in shared memory and written as fp32
-// qa/ka [B, h, s1, D].  HBM-bound: the algorithmic traffic is the single read
-// of q and k plus the (small) fp32 means.
+// the four partial sums are combined in shared memory.  Each mean m is written
+// as two tf32 values, hi = m rounded to tf32 and lo = (m - hi) rounded to tf32
+// ([B, h, s1, D] each), the operands of the three-term tf32 pooled-map GEMM.
+// HBM-bound: the algorithmic traffic is the single read of q and k plus the
+// (small) means.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -57,12 +59,19 @@ struct Chunk<__nv_bfloat16> {
   }
 };
 
+__device__ __forceinline__ float to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 // grid: (s1, ceil(C / 64), 2 * B); C = h*D / elems-per-chunk.  z selects (b, q|k).
+// qa/ka point at the hi arrays; the lo arrays follow at +lo_off elements.
 template <typename T>
 __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
                                                    const T *__restrict__ k, int S, int h, int D,
                                                    float *__restrict__ qa,
-                                                   float *__restrict__ ka) {
+                                                   float *__restrict__ ka, size_t lo_off) {
   constexpr int E = Chunk<T>::kElems;
   __shared__ float part[kRowGroups][kChunksPerCta * E];
 
@@ -100,27 +109,30 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
   for (int e = threadIdx.x; e < kChunksPerCta * E; e += blockDim.x) {
     const int col = blockIdx.y * kChunksPerCta * E + e;
     if (col >= row_elems) break;
-    float s = part[0][e] + part[1][e] + part[2][e] + part[3][e];
+    const float m = (part[0][e] + part[1][e] + part[2][e] + part[3][e]) * (1.0f / 64.0f);
     const int hh = col / D, d = col - hh * D;
-    dst[(((size_t)b * h + hh) * s1 + i) * D + d] = s * (1.0f / 64.0f);
+    const size_t at = (((size_t)b * h + hh) * s1 + i) * D + d;
+    const float hi = to_tf32(m);
+    dst[at] = hi;
+    dst[at + lo_off] = to_tf32(m - hi);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
-                        float *ka, cudaStream_t st) {
+                        float *ka, size_t lo_off, cudaStream_t st) {
   const int E = dt == NABLA_BF16 ? 8 : 4;
   const int C = s.h * s.D / E;
   dim3 grid(s.s1, (C + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
   if (dt == NABLA_BF16)
     pool_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), s.S, s.h,
-        s.D, qa, ka);
+        s.D, qa, ka, lo_off);
   else
     pool_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(q),
                                              static_cast<const float *>(k), s.S, s.h, s.D, qa,
-                                             ka);
+                                             ka, lo_off);
   return cudaGetLastError();
 }
 

@@ -1,5 +1,6 @@
 // The library's device status word: kernels record a bounded wait that gave up
 // or an out-of-range block index here (first writer wins) instead of trapping.
+// Also the shared lookup of the driver's tensor-map encoder.
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -45,6 +46,23 @@ int *device_status_ptr(cudaError_t *err) {
 cudaError_t launch_bounded_wait_probe(cudaStream_t st) {
   bounded_wait_probe<<<1, 32, 0, st>>>(20000000ull);  // 20 ms
   return cudaGetLastError();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder(cudaError_t *err) {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    *err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                            cudaEnableDefault, &q);
+    if (*err != cudaSuccess || q != cudaDriverEntryPointSuccess || !p) {
+      if (*err == cudaSuccess) *err = cudaErrorNotSupported;
+      return nullptr;
+    }
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *err = cudaSuccess;
+  return fn;
 }
 
 }  // namespace nabla

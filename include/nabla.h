@@ -66,9 +66,10 @@ int nabla_abi_version(void);
 const char *nabla_status_string(nabla_status s);
 
 /*
- * Scratch bytes nabla_build_mask needs for a shape: the fp32 block means of q
- * and k ([B, h, s1, D] each) and the fp32 pooled map ([B, h, s1, s1]), each
- * region 256-byte aligned.  Returns 0 for an invalid shape.
+ * Scratch bytes nabla_build_mask needs for a shape: the block means of q and k
+ * as tf32 hi/lo pairs (four fp32 [B, h, s1, D] arrays) and the fp32 pooled map
+ * ([B, h, s1, s1]), each region 256-byte aligned.  Returns 0 for an invalid
+ * shape.
  */
 size_t nabla_build_mask_workspace_bytes(int B, int S, int h, int D);
 

@@ -58,8 +58,8 @@ def _ws(B, S, h, D):
     def up(x):
         return (x + 255) // 256 * 256
 
-    means = B * h * s1 * D * 4
-    return up(up(up(means) + means) + B * h * s1 * s1 * 4)
+    means = up(B * h * s1 * D * 4)
+    return up(4 * means + B * h * s1 * s1 * 4)
 
 
 @pytest.mark.parametrize("shape", [(1, 1024, 2, 64), (1, 98304, 24, 128), (2, 64 * 37, 3, 128)])
