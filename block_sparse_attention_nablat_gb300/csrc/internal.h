@@ -39,7 +39,8 @@ MaskWorkspace mask_workspace_layout(const Shape &s);
 // each [B, h, s1, D].
 cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
                         float *ka, size_t lo_off, cudaStream_t st);
-// K2a: pooled map L = qa ka^T / sqrt(D), fp32 [B, h, s1, s1], on tcgen05 (3-term tf32).
+// K2a: pooled map in base-2 units, L = qa ka^T log2(e) / sqrt(D), fp32 [B, h, s1, s1],
+// on tcgen05 (3-term tf32).
 cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const float *ka_hi,
                               const float *ka_lo, const Shape &s, float *L, int *status,
                               cudaStream_t st);

@@ -18,7 +18,9 @@
 // K = D streamed in 32-column (128-byte swizzled) chunks of the four operands
 // through a 2-stage TMA ring; the accumulator lives in TMEM (two 256-column
 // buffers, so the epilogue of one tile overlaps the MMAs of the next); the
-// epilogue (thread = row) scales by 1/sqrt(D) and stores fp32 rows.  Operand
+// epilogue scales by log2(e)/sqrt(D) -- the map is kept in base-2 units, so
+// the softmax that follows is a plain 2^x -- and writes fp32 rows, transposed
+// through shared memory into 128-byte row segments.  Operand
 // tensors are 3-D (D, s1, B*h) so a tile never reads across a head boundary
 // (out-of-range rows are zero-filled and their results are not stored).
 #include <cuda.h>
@@ -44,12 +46,15 @@ constexpr int kThreads = 256;
 constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                             ((uint32_t)(kBM >> 4) << 24);
 
+constexpr int kStagePad = 33;  // 32 x 33 fp32 per epilogue warp: conflict-free transpose
+
 struct MapSync {
   uint64_t full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain;
   uint32_t tmem_slot;
   int abort;
 };
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + (int)sizeof(MapSync);
+constexpr int kTransBytes = 4 * 32 * kStagePad * 4;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kTransBytes + (int)sizeof(MapSync);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -85,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  MapSync *sync = reinterpret_cast<MapSync *>(smem + kStages * kStageBytes);
+  float *trans = reinterpret_cast<float *>(smem + kStages * kStageBytes);
+  MapSync *sync = reinterpret_cast<MapSync *>(smem + kStages * kStageBytes + kTransBytes);
   volatile int *abort = &sync->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long tiles = (long)P.bh * P.mt * P.nt;
@@ -167,11 +173,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&sync->drain);
     mbar_wait(&sync->drain, 0, nullptr, P.status, kDevTimeout);
   } else if (warp >= 4) {
-    // ---- epilogue: thread = accumulator lane = tile row
+    // ---- epilogue: thread = accumulator lane = tile row.  Each warp owns 32 rows;
+    // every 32-column piece is transposed through shared memory so that each
+    // store instruction writes one contiguous 128-byte segment of one row.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const bool vec = (P.s1 & 3) == 0;
+    float *tw = trans + q4 * 32 * kStagePad;
     uint32_t tc = 0;
     for (long t = blockIdx.x; t < tiles && !*abort; t += gridDim.x, ++tc) {
       const uint32_t ab = tc & 1u;
@@ -181,30 +189,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int bh = (int)(t / (P.mt * P.nt));
       const int rem = (int)(t - (long)bh * P.mt * P.nt);
-      const int row = (rem / P.nt) * kBM + r, n0 = (rem % P.nt) * kBN;
-      float *out = P.L + ((size_t)bh * P.s1 + row) * P.s1;
+      const int row0 = (rem / P.nt) * kBM + q4 * 32, n0 = (rem % P.nt) * kBN;
+      (void)r;
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + ab * 256 + c * 32, v);
         tmem_wait_ld();
         reg_fence(v);
-        const int col = n0 + c * 32;
-        if (row < P.s1 && col < P.s1) {
-          if (vec && col + 32 <= P.s1) {
-            float4 *dst = reinterpret_cast<float4 *>(out + col);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(v[4 * i]) * P.scale,
-                                   __uint_as_float(v[4 * i + 1]) * P.scale,
-                                   __uint_as_float(v[4 * i + 2]) * P.scale,
-                                   __uint_as_float(v[4 * i + 3]) * P.scale);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col + i < P.s1) out[col + i] = __uint_as_float(v[i]) * P.scale;
-          }
+        for (int i = 0; i < 32; ++i) tw[lane * kStagePad + i] = __uint_as_float(v[i]) * P.scale;
+        __syncwarp();
+        const int col = n0 + c * 32 + lane;
+        if (col < P.s1) {
+          float *out = P.L + ((size_t)bh * P.s1 + row0) * P.s1 + col;
+#pragma unroll 4
+          for (int rr = 0; rr < 32; ++rr)
+            if (row0 + rr < P.s1) out[(size_t)rr * P.s1] = tw[rr * kStagePad + lane];
         }
+        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(&sync->acc_empty[ab]);
@@ -252,7 +255,7 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
                                   kSmemBytes)) != cudaSuccess)
     return err;
   MapParams p{L, s.B * s.h, s.s1, s.D, (s.s1 + kBM - 1) / kBM, (s.s1 + kBN - 1) / kBN,
-              (float)(1.0 / sqrt((double)s.D)), status};
+              (float)(1.4426950408889634 / sqrt((double)s.D)), status};
   const long tiles = (long)p.bh * p.mt * p.nt;
   const int grid = (int)(tiles < sms ? tiles : sms);
   pooled_map_kernel<<<grid, kThreads, kSmemBytes, st>>>(tQh, tQl, tKh, tKl, p);
