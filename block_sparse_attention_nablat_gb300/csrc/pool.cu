@@ -24,11 +24,18 @@ constexpr int kChunksPerCta = 64;
 constexpr int kRowGroups = 4;
 constexpr int kRowsPerThread = 64 / kRowGroups;
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+// q and k are read once: evict-first in L2, so that the stream does not push
+// out the pooled map and means that the following kernels read back from L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p, uint64_t pol) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return r;
 }
 
@@ -65,12 +72,13 @@ __device__ __forceinline__ float to_tf32(float x) {
   return __uint_as_float(r);
 }
 
-// grid: (s1, ceil(C / 64), 2 * B); C = h*D / elems-per-chunk.  z selects (b, q|k).
+// grid: (s1, ceil((c1 - c0) / 64), 2 * B); chunks [c0, c1) of the h*D row (the
+// heads of one group; C = h*D / elems-per-chunk in all).  z selects (b, q|k).
 // qa/ka point at the hi arrays; the lo arrays follow at +lo_off elements.
 template <typename T>
 __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
                                                    const T *__restrict__ k, int S, int h, int D,
-                                                   float *__restrict__ qa,
+                                                   int c0, int c1, float *__restrict__ qa,
                                                    float *__restrict__ ka, size_t lo_off) {
   constexpr int E = Chunk<T>::kElems;
   __shared__ float part[kRowGroups][kChunksPerCta * E];
@@ -82,20 +90,22 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
   const int C = h * D / E;
   const int cx = threadIdx.x % kChunksPerCta;
   const int rg = threadIdx.x / kChunksPerCta;
-  const int c = blockIdx.y * kChunksPerCta + cx;
+  const int cb = c0 + blockIdx.y * kChunksPerCta;  // first chunk of this CTA
+  const int c = cb + cx;
 
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
 
-  if (c < C) {
+  if (c < c1) {
+    const uint64_t pol = evict_first_policy();
     const T *src = is_k ? k : q;
     const uint4 *base =
         reinterpret_cast<const uint4 *>(src + ((size_t)b * S + (size_t)i * 64) * h * D) + c;
     uint4 v[kRowsPerThread];
 #pragma unroll
     for (int r = 0; r < kRowsPerThread; ++r)
-      v[r] = ld_stream(base + (size_t)(rg + kRowGroups * r) * C);
+      v[r] = ld_stream(base + (size_t)(rg + kRowGroups * r) * C, pol);
 #pragma unroll
     for (int r = 0; r < kRowsPerThread; ++r) Chunk<T>::add(acc, v[r]);
   }
@@ -105,10 +115,9 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
 
   // 64 chunks * E elements per CTA, spread over the 256 threads.
   float *dst = is_k ? ka : qa;
-  const int row_elems = h * D;
   for (int e = threadIdx.x; e < kChunksPerCta * E; e += blockDim.x) {
-    const int col = blockIdx.y * kChunksPerCta * E + e;
-    if (col >= row_elems) break;
+    const int col = cb * E + e;
+    if (col >= c1 * E) break;
     const float m = (part[0][e] + part[1][e] + part[2][e] + part[3][e]) * (1.0f / 64.0f);
     const int hh = col / D, d = col - hh * D;
     const size_t at = (((size_t)b * h + hh) * s1 + i) * D + d;
@@ -120,19 +129,19 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
 
 }  // namespace
 
-cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, float *qa,
-                        float *ka, size_t lo_off, cudaStream_t st) {
-  const int E = dt == NABLA_BF16 ? 8 : 4;
-  const int C = s.h * s.D / E;
-  dim3 grid(s.s1, (C + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
+cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, int h0,
+                        int h1, float *qa, float *ka, size_t lo_off, cudaStream_t st) {
+  const int E = dt == NABLA_BF16 ? 8 : 4;  // D is a multiple of 64: heads start on a chunk
+  const int c0 = h0 * s.D / E, c1 = h1 * s.D / E;
+  dim3 grid(s.s1, (c1 - c0 + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
   if (dt == NABLA_BF16)
     pool_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), s.S, s.h,
-        s.D, qa, ka, lo_off);
+        s.D, c0, c1, qa, ka, lo_off);
   else
     pool_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(q),
-                                             static_cast<const float *>(k), s.S, s.h, s.D, qa,
-                                             ka, lo_off);
+                                             static_cast<const float *>(k), s.S, s.h, s.D, c0,
+                                             c1, qa, ka, lo_off);
   return cudaGetLastError();
 }
 

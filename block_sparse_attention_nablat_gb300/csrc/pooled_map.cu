@@ -77,11 +77,19 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
 
 struct MapParams {
   float *L;
-  int bh, s1, D;
+  int h, h0, nh;  // heads per batch; this launch covers heads [h0, h0 + nh) of every batch
+  int units;      // B * nh (batch, head) pairs
+  int s1, D;
   int mt, nt;  // tiles along rows / columns of one head
   float scale;
   int *status;
 };
+
+// (batch * h + head) of the u-th (batch, head) pair of a launch.
+__device__ __forceinline__ int pair_index(const MapParams &P, int u) {
+  const int b = u / P.nh;
+  return b * P.h + P.h0 + (u - b * P.nh);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     pooled_map_kernel(const __grid_constant__ CUtensorMap tQh, const __grid_constant__ CUtensorMap tQl,
@@ -94,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   MapSync *sync = reinterpret_cast<MapSync *>(smem + kStages * kStageBytes + kTransBytes);
   volatile int *abort = &sync->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long tiles = (long)P.bh * P.mt * P.nt;
+  const long tiles = (long)P.units * P.mt * P.nt;
   const int chunks = P.D / kBK;
 
   if (threadIdx.x == 0) {
@@ -120,8 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- TMA producer
     uint32_t it = 0;
     for (long t = blockIdx.x; t < tiles && !*abort; t += gridDim.x) {
-      const int bh = (int)(t / (P.mt * P.nt));
-      const int rem = (int)(t - (long)bh * P.mt * P.nt);
+      const int u = (int)(t / (P.mt * P.nt));
+      const int rem = (int)(t - (long)u * P.mt * P.nt);
+      const int bh = pair_index(P, u);
       const int m0 = (rem / P.nt) * kBM, n0 = (rem % P.nt) * kBN;
       for (int c = 0; c < chunks; ++c, ++it) {
         const uint32_t st = it % kStages, ph = (it / kStages) & 1u;
@@ -187,8 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                         P.status, kDevTimeout));
       if (!ok) break;
       tc_fence_after();
-      const int bh = (int)(t / (P.mt * P.nt));
-      const int rem = (int)(t - (long)bh * P.mt * P.nt);
+      const int u = (int)(t / (P.mt * P.nt));
+      const int rem = (int)(t - (long)u * P.mt * P.nt);
+      const int bh = pair_index(P, u);
       const int row0 = (rem / P.nt) * kBM + q4 * 32, n0 = (rem % P.nt) * kBN;
       (void)r;
 #pragma unroll 1
@@ -238,8 +248,8 @@ bool make_map3(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const floa
 }  // namespace
 
 cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const float *ka_hi,
-                              const float *ka_lo, const Shape &s, float *L, int *status,
-                              cudaStream_t st) {
+                              const float *ka_lo, const Shape &s, int h0, int h1, float *L,
+                              int *status, cudaStream_t st) {
   cudaError_t err;
   auto enc = tensor_map_encoder(&err);
   if (!enc) return err;
@@ -254,9 +264,18 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
   if ((err = cudaFuncSetAttribute(pooled_map_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   kSmemBytes)) != cudaSuccess)
     return err;
-  MapParams p{L, s.B * s.h, s.s1, s.D, (s.s1 + kBM - 1) / kBM, (s.s1 + kBN - 1) / kBN,
-              (float)(1.4426950408889634 / sqrt((double)s.D)), status};
-  const long tiles = (long)p.bh * p.mt * p.nt;
+  MapParams p{L,
+              s.h,
+              h0,
+              h1 - h0,
+              s.B * (h1 - h0),
+              s.s1,
+              s.D,
+              (s.s1 + kBM - 1) / kBM,
+              (s.s1 + kBN - 1) / kBN,
+              (float)(1.4426950408889634 / sqrt((double)s.D)),
+              status};
+  const long tiles = (long)p.units * p.mt * p.nt;
   const int grid = (int)(tiles < sms ? tiles : sms);
   pooled_map_kernel<<<grid, kThreads, kSmemBytes, st>>>(tQh, tQl, tKh, tKl, p);
   return cudaGetLastError();

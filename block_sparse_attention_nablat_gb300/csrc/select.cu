@@ -8,27 +8,29 @@
 // "Hybrid Integration with STA".
 //
 // The pooled map arrives in base-2 units (L * log2 e, folded into the map's
-// scale), so p = 2^(L - max) / sum.  One warp per row; the row (s1 <= 2048
-// values) lives in registers, lane l holding the float4 groups at columns
-// 128 m + 4 l .. 128 m + 4 l + 3.  The page sorts the row, but the kept set is
-// a suffix of the ascending (p, index) order, so only the cut point is needed.
-// With key(j) = float bits of p_j (monotone since p >= 0):
-//   1. radix passes over the key range: 32 buckets per pass, each lane adding
-//      its blocks' mass and count into its own column of a [bucket][lane]
-//      shared-memory table (no atomics, no bank conflicts); the warp sums the
-//      columns, scans the 32 bucket masses and keeps the bucket in which the
-//      running sum first reaches t = 1 - thr;
-//   2. as soon as that bucket holds at most 64 blocks, they are compacted into
-//      shared memory as 32-bit (key - bucket start, index) pairs, sorted by a
-//      warp bitonic network and scanned from the mass below the bucket, which
-//      gives the exact cut: the first pair (K, i*) whose running sum is >= t;
-//   3. a bucket that shrinks to a single key is a run of exact ties: their
-//      running sums are base + r * p, so the first kept rank follows directly.
+// scale).  One warp per row; the row (s1 <= 2048 values) lives in registers,
+// lane l holding the float4 groups at columns 128 m + 4 l .. 128 m + 4 l + 3.
+// The softmax is left unnormalised: e_j = 2^(L_j - max), Z = sum e, and the
+// running sum of p = e / Z reaches t = 1 - thr exactly where the running sum
+// of e reaches t Z, so the cut is taken on e against t Z.  The page sorts the
+// row, but the kept set is a suffix of the ascending (e, index) order, so only
+// the cut point is needed.  With key(j) = float bits of e_j (monotone, e >= 0):
+//   1. one radix pass over the register-resident row: 32 buckets over the key
+//      range, each lane adding its blocks' mass into its own column of a
+//      [bucket][lane] table; the warp sums the columns, scans the bucket
+//      masses and keeps the bucket in which the running sum first reaches t Z;
+//   2. the blocks of that bucket (typically a tenth of the row) are copied into
+//      a lane-private list in shared memory; further 32-bucket passes run on
+//      the list alone until the bucket holds at most 64 blocks;
+//   3. those blocks, as 32-bit (key - bucket start, index) pairs, give the
+//      exact cut: the first pair (K, i*) in ascending order whose running sum
+//      is >= t Z -- by a rank count when they fit one per lane, else by a warp
+//      bitonic sort.  A bucket that shrinks to a single key is a run of exact
+//      ties, whose running sums base + r e_K give the first kept rank directly.
 // Block j is then kept iff key(j) > K, or key(j) == K and j is at or after
 // the cut in index order -- the kept set of the sort-based definition,
 // evaluated in fp32.  Kept indices, ORed with the STA row, are written in
-// ascending order: per 128-column group, four warp ballots give every lane its
-// output position by population counts.
+// ascending order; one packed warp scan gives the offsets of four groups.
 #include <cfloat>
 
 #include "internal.h"
@@ -36,43 +38,35 @@
 namespace nabla {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
 constexpr int kBuckets = 32;
+constexpr int kSlots = 16;  // lane-private list entries per lane
 constexpr int kMaxCand = 64;
+constexpr unsigned kAll = 0xffffffffu;
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(kAll, x, o));
   return x;
 }
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-__device__ __forceinline__ uint32_t warp_umin(uint32_t x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x = min(x, __shfl_xor_sync(0xffffffffu, x, o));
-  return x;
-}
-__device__ __forceinline__ uint32_t warp_umax(uint32_t x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x = max(x, __shfl_xor_sync(0xffffffffu, x, o));
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(kAll, x, o);
   return x;
 }
 // inclusive prefix sums over the lanes
 __device__ __forceinline__ float warp_scan(float x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    const float y = __shfl_up_sync(kAll, x, o);
     if (lane >= o) x += y;
   }
   return x;
 }
-__device__ __forceinline__ int warp_scan_i(int x, int lane) {
+__device__ __forceinline__ uint32_t warp_scan_u(uint32_t x, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const uint32_t y = __shfl_up_sync(kAll, x, o);
     if (lane >= o) x += y;
   }
   return x;
@@ -85,62 +79,151 @@ __device__ __forceinline__ float exp2_approx(float x) {
 }
 
 struct WarpScratch {
-  float mass[kBuckets][33];       // [bucket][lane] (+1 pad): lane-private columns
-  uint32_t count[kBuckets / 4][33];  // byte b & 3 of word [b >> 2][lane]: a lane holds <= 64 blocks
-  uint32_t cand[kMaxCand];   // ((key - bucket start) << 11) | index
+  float mass[kBuckets + 1][32];          // [bucket][lane]: lane-private columns; last row: sink
+  uint32_t count[kBuckets / 2 + 1][32];  // 16-bit fields: bucket 2w (low), 2w + 1 (high)
+  uint32_t list_key[kSlots + 1][32];     // [slot][lane]; last row: sink
+  uint16_t list_idx[kSlots + 1][32];     // block index of the entry (separate array: a 64-bit
+                                         // store would tie every key register to a pair)
+  uint32_t cand[kMaxCand];
 };
 
-// Ascending bitonic sort of 64 32-bit keys held two per lane (positions lane, lane+32).
-__device__ __forceinline__ void warp_sort64(uint32_t &a, uint32_t &b, int lane) {
+// The cut range [lo, hi) of keys, the mass below it, and how many blocks it holds.
+struct Range {
+  uint32_t lo, hi;
+  float base;
+  int n;
+};
+
+// Sum of the lane columns of bucket `lane`: eight 16-byte reads, each quarter
+// warp reading eight different 16-byte columns (no bank conflicts).
+__device__ __forceinline__ float column_mass(const WarpScratch &ws, int lane) {
+  const float4 *row = reinterpret_cast<const float4 *>(ws.mass[lane]);
+  float s = 0.f;
+#pragma unroll 1
+  for (int k0 = 0; k0 < 8; k0 += 4) {  // four loads in flight: the row stays in registers
 #pragma unroll
-  for (int k = 2; k <= 64; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j == 32) {  // partners are the two values of one lane; k == 64 ascends everywhere
-        const uint32_t lo = min(a, b), hi = max(a, b);
-        a = lo;
-        b = hi;
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t &x = h ? b : a;
-          const int pos = lane + 32 * h;
-          const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
-          // the lower position of a pair keeps the smaller key in an ascending run
-          const bool take_min = ((pos & j) == 0) == ((pos & k) == 0);
-          x = take_min ? min(x, y) : max(x, y);
-        }
-      }
+    for (int k = k0; k < k0 + 4; ++k) {
+      const float4 v = row[(k + lane) & 7];
+      s += (v.x + v.y) + (v.z + v.w);
     }
   }
+  return s;
+}
+__device__ __forceinline__ int column_count(const WarpScratch &ws, int lane) {
+  const uint4 *row = reinterpret_cast<const uint4 *>(ws.count[lane >> 1]);
+  uint32_t s = 0u;
+#pragma unroll 1
+  for (int k0 = 0; k0 < 8; k0 += 4) {
+#pragma unroll
+    for (int k = k0; k < k0 + 4; ++k) {
+      const uint4 v = row[(k + (lane >> 1)) & 7];
+      s += (v.x + v.y) + (v.z + v.w);
+    }
+  }
+  return (int)((s >> (16 * (lane & 1))) & 0xffffu);
+}
+
+// Narrow r to the bucket (of 2^sh keys, bucket 0 starting at d0 << sh) in which
+// base + running mass first reaches tz; returns the bucket index.  If fp32
+// rounding leaves the sums just short of tz, the cut falls in the last bucket
+// with mass (the heaviest block is always kept: the whole row sums to Z > tz).
+__device__ __forceinline__ int choose_bucket(Range &r, float bmass, float tz, int sh, uint32_t d0,
+                                             int lane) {
+  const float cum = warp_scan(bmass, lane);
+  const unsigned reach = __ballot_sync(kAll, r.base + cum >= tz);
+  const unsigned heavy = __ballot_sync(kAll, bmass > 0.f);
+  const int bs = reach   ? __ffs(reach) - 1
+                 : heavy ? 31 - __clz(heavy)
+                         : (int)(((r.hi - 1u) >> sh) - d0);
+  r.base += __shfl_sync(kAll, cum - bmass, bs);
+  r.lo = max(r.lo, (d0 + (uint32_t)bs) << sh);
+  r.hi = min(r.hi, (d0 + (uint32_t)bs + 1u) << sh);
+  return bs;
+}
+
+// Bucket width for a range: 32 buckets of 2^sh keys cover [lo, hi).
+__device__ __forceinline__ int bucket_shift(const Range &r) {
+  const int top = 31 - __clz(r.lo ^ (r.hi - 1u));
+  return top > 4 ? top - 4 : 0;
+}
+
+// One 32-bucket pass over the register-resident row (element e of group m is
+// column 128 m + 4 lane + e), then the choice of the cut bucket.  RANGED: only
+// keys in [r.lo, r.hi) count; the first pass covers every key and needs no
+// test.  Excluded elements add into the sink row, so the loop has no branches.
+template <int NV, bool FULL, bool RANGED>
+__device__ __forceinline__ void register_pass(WarpScratch &ws, const float (&p)[NV][4], Range &r,
+                                              float tz, int lane, int nv, int s1) {
+  const int sh = bucket_shift(r);
+  const uint32_t d0 = r.lo >> sh, lo = r.lo, w = r.hi - r.lo;
+#pragma unroll
+  for (int b = 0; b < kBuckets; ++b) ws.mass[b][lane] = 0.f;
+#pragma unroll
+  for (int m = 0; m < NV; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t u = __float_as_uint(p[m][e]);
+      bool in = FULL || (m < nv && 128 * m + 4 * lane + e < s1);
+      if (RANGED) in = in && u - lo < w;
+      const uint32_t b = in ? (u >> sh) - d0 : (uint32_t)kBuckets;
+      ws.mass[b][lane] += p[m][e];
+    }
+  __syncwarp();
+  const float bmass = column_mass(ws, lane);
+  __syncwarp();
+  choose_bucket(r, bmass, tz, sh, d0, lane);
+}
+
+// Copy the blocks with keys in [r.lo, r.hi) into this lane's list and return
+// how many there are; past kSlots - 1 they overwrite the last slot (overflow,
+// detected by the caller), and the others write the sink row.
+template <int NV, bool FULL>
+__device__ __forceinline__ int compact_range(WarpScratch &ws, const float (&p)[NV][4],
+                                             const Range &r, int lane, int nv, int s1) {
+  const uint32_t lo = r.lo, w = r.hi - r.lo;
+  int c = 0;
+#pragma unroll
+  for (int m = 0; m < NV; ++m)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t u = __float_as_uint(p[m][e]);
+      const int j = 128 * m + 4 * lane + e;
+      const bool in = (FULL || (m < nv && j < s1)) && u - lo < w;
+      const int slot = in ? min(c, kSlots - 1) : kSlots;
+      ws.list_key[slot][lane] = u;
+      ws.list_idx[slot][lane] = (uint16_t)j;
+      c += in ? 1 : 0;
+    }
+  return c;
 }
 
 // NV = float4 groups per lane (s1 <= 128 * NV); FULL: s1 == 128 * NV exactly,
 // so no column needs a bounds check.
+// Rows: grid.y = batch b; the launch covers rows [row0, row0 + nrows) of every
+// batch (the heads of one group), a batch being bstride = h * s1 rows apart.
 template <int NV, bool FULL>
-__global__ void __launch_bounds__(kWarps * 32) select_kernel(const float *__restrict__ L,
-                                                             long rows, int s1,
-                                                             const uint8_t *__restrict__ sta,
-                                                             bool sta_words, float t,
-                                                             int32_t *__restrict__ kv_nb,
-                                                             int32_t *__restrict__ kv_inds) {
+__global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
+    select_kernel(const float *__restrict__ L, long row0, long bstride, int nrows, int s1,
+                  const uint8_t *__restrict__ sta, bool sta_words, float t,
+                  int32_t *__restrict__ kv_nb, int32_t *__restrict__ kv_inds) {
   __shared__ WarpScratch scratch[kWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long row = (long)blockIdx.x * kWarps + warp;
-  if (row >= rows) return;  // uniform per warp
+  const int local = blockIdx.x * kWarps + warp;
+  if (local >= nrows) return;  // uniform per warp
+  const long row = blockIdx.y * bstride + row0 + local;
   WarpScratch &ws = scratch[warp];
   const int i = (int)(row % s1);
   const float *Lr = L + row * s1;
   const int nv = FULL ? NV : (s1 + 127) >> 7;
-  const bool vec = FULL || (s1 & 3) == 0;
   auto valid = [&](int m, int e) { return FULL || (m < nv && 128 * m + 4 * lane + e < s1); };
+  const unsigned lt_mask = (1u << lane) - 1u;
 
   // ---- load the row; column of element e of group m is 128 m + 4 lane + e
   float p[NV][4];
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
     const int j0 = 128 * m + 4 * lane;
-    if (FULL || (m < nv && vec && j0 + 3 < s1)) {
+    if (FULL || (m < nv && (s1 & 3) == 0 && j0 + 3 < s1)) {
       const float4 v = *reinterpret_cast<const float4 *>(Lr + j0);
       p[m][0] = v.x;
       p[m][1] = v.y;
@@ -151,166 +234,196 @@ __global__ void __launch_bounds__(kWarps * 32) select_kernel(const float *__rest
       for (int e = 0; e < 4; ++e) p[m][e] = valid(m, e) ? Lr[j0 + e] : -FLT_MAX;
     }
   }
-  // ---- softmax (fp32, base 2)
+  // ---- unnormalised softmax e = 2^(L - max) (fp32); Z = sum e
   float mx = -FLT_MAX;
 #pragma unroll
   for (int m = 0; m < NV; ++m)
     mx = fmaxf(mx, fmaxf(fmaxf(p[m][0], p[m][1]), fmaxf(p[m][2], p[m][3])));
   mx = warp_max(mx);
-  float z0 = 0.f, z1 = 0.f;
+  float z0 = 0.f, z1 = 0.f, emin = FLT_MAX, emax = 0.f;
 #pragma unroll
   for (int m = 0; m < NV; ++m)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      p[m][e] = valid(m, e) ? exp2_approx(p[m][e] - mx) : 0.f;
+      if (valid(m, e)) {
+        // fmaxf maps a NaN (from non-finite logits) to 0: every key then lies in
+        // [kmin, kmax], which bounds the bucket indices of the first pass
+        p[m][e] = fmaxf(exp2_approx(p[m][e] - mx), 0.f);
+        emin = fminf(emin, p[m][e]);
+        emax = fmaxf(emax, p[m][e]);
+      } else {
+        p[m][e] = 0.f;
+      }
       if (e & 1)
         z1 += p[m][e];
       else
         z0 += p[m][e];
     }
-  const float inv_z = 1.0f / warp_sum(z0 + z1);
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll
-  for (int m = 0; m < NV; ++m)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      p[m][e] *= inv_z;
-      if (valid(m, e)) {
-        const uint32_t u = __float_as_uint(p[m][e]);
-        kmin = min(kmin, u);
-        kmax = max(kmax, u);
-      }
-    }
-  kmin = warp_umin(kmin);
-  kmax = warp_umax(kmax);
+  const float tz = t * warp_sum(z0 + z1);
+  // e >= 0, so float order is the order of the bits
+  const uint32_t kmin = __reduce_min_sync(kAll, __float_as_uint(emin));
+  const uint32_t kmax = __reduce_max_sync(kAll, __float_as_uint(emax));
 
   // ---- cut: kept iff key > K, or key == K and tie rank (index order) >= R
+  const bool keep_all = !(t > 0.f);
   uint32_t K = 0u;
   int R = 0;
   int ties_at_K = 2;  // > 1 unless the cut key is known to be unique
-  if (t > 0.f) {
-    uint32_t lo = kmin, hi = kmax + 1u;
-    float base = 0.f;  // mass of keys below lo
-    int in_range = s1;  // blocks with key in [lo, hi)
-    // each pass takes 5 bits off a range of < 2^30 keys: 7 passes always suffice
-    for (int pass = 0; pass < 7; ++pass) {
-      if (hi - lo == 1u) {  // a single key: a run of exact ties
-        // running sums base + (r + 1) pk at tie ranks r = 0 .. in_range - 1
-        const float pk = __uint_as_float(lo);
-        K = lo;
-        R = pk > 0.f ? min(max(0, (int)ceilf((t - base) / pk) - 1), in_range - 1) : 0;
-        ties_at_K = in_range;
+  if (!keep_all) {
+    Range r{kmin, kmax + 1u, 0.f, s1};
+    bool done = false;
+    // a bucket of one key is a run of exact ties: running sums base + (r + 1) e_K
+    // at tie ranks r = 0 .. n - 1
+    auto finish_ties = [&](const Range &rr) {
+      const float ek = __uint_as_float(rr.lo);
+      K = rr.lo;
+      R = ek > 0.f ? min(max(0, (int)ceilf((tz - rr.base) / ek) - 1), rr.n - 1) : 0;
+      ties_at_K = rr.n;
+      done = true;
+    };
+    int c = 0;  // this lane's list entries (more than kSlots: overflow)
+    if (r.hi - r.lo == 1u) {
+      finish_ties(r);
+    } else {
+      register_pass<NV, FULL, false>(ws, p, r, tz, lane, nv, s1);
+      c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
+      r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
+      // rare: the cut bucket overflows a lane's list; narrow it in registers
+#pragma unroll 1
+      for (int level = 1; !done && (int)__reduce_max_sync(kAll, (unsigned)c) > kSlots; ++level) {
+        if (r.hi - r.lo == 1u) {
+          finish_ties(r);
+        } else if (level == 7) {  // unreachable: each pass takes 5 bits off a < 2^30 range
+          K = r.lo;
+          R = 0;
+          done = true;
+        } else {
+          register_pass<NV, FULL, true>(ws, p, r, tz, lane, nv, s1);
+          c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
+          r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
+        }
+      }
+    }
+    // -- passes over the list
+    const int nl = min(c, kSlots);
+    const int cmax = (int)__reduce_max_sync(kAll, (unsigned)nl);
+#pragma unroll 1
+    for (int pass = 0; pass < 8 && !done; ++pass) {
+      if (r.n <= kMaxCand && r.hi - r.lo <= (1u << 21)) {
+        // ---- exact finish: (key - lo) packs with an 11-bit block index
+        const uint32_t lo = r.lo, w = r.hi - r.lo;
+        int nc = 0;
+#pragma unroll 1
+        for (int sl = 0; sl < cmax; ++sl) {
+          const uint32_t key = ws.list_key[sl][lane];
+          const bool in = sl < nl && key - lo < w;
+          const unsigned bal = __ballot_sync(kAll, in);
+          const int at = nc + __popc(bal & lt_mask);
+          if (in && at < kMaxCand) ws.cand[at] = ((key - lo) << 11) | ws.list_idx[sl][lane];
+          nc += __popc(bal);
+        }
+        nc = min(nc, kMaxCand);
+        __syncwarp();
+        if (nc <= 32) {
+          // rank count: running sum at a pair = base + mass of the pairs below it
+          const uint32_t my = lane < nc ? ws.cand[lane] : kAll;
+          const float ev = lane < nc ? __uint_as_float((my >> 11) + lo) : 0.f;
+          float below = 0.f;
+#pragma unroll 4
+          for (int sl = 0; sl < nc; ++sl) {
+            const uint32_t o = __shfl_sync(kAll, my, sl);
+            const float eo = __shfl_sync(kAll, ev, sl);
+            if (o < my) below += eo;
+          }
+          const bool reach = lane < nc && r.base + below + ev >= tz;
+          uint32_t cut = __reduce_min_sync(kAll, reach ? my : kAll);
+          if (cut == kAll) cut = __reduce_max_sync(kAll, lane < nc ? my : 0u);  // keep the heaviest
+          const uint32_t kd = cut >> 11;
+          K = kd + lo;
+          R = __popc(__ballot_sync(kAll, lane < nc && (my >> 11) == kd && my < cut));
+          ties_at_K = __popc(__ballot_sync(kAll, lane < nc && (my >> 11) == kd));
+        } else {
+          // ascending bitonic sort of 64 keys held two per lane (positions lane, lane + 32)
+          uint32_t a = ws.cand[lane];
+          uint32_t b = lane + 32 < nc ? ws.cand[lane + 32] : kAll;
+#pragma unroll
+          for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+              if (j == 32) {  // partners are the two values of one lane; k == 64 ascends
+                const uint32_t x = min(a, b), y = max(a, b);
+                a = x;
+                b = y;
+              } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  uint32_t &x = h ? b : a;
+                  const int pos = lane + 32 * h;
+                  const uint32_t y = __shfl_xor_sync(kAll, x, j);
+                  const bool take_min = ((pos & j) == 0) == ((pos & k) == 0);
+                  x = take_min ? min(x, y) : max(x, y);
+                }
+              }
+            }
+          }
+          const float pa = __uint_as_float((a >> 11) + lo);  // nc > 32: position lane is real
+          const float pb = lane + 32 < nc ? __uint_as_float((b >> 11) + lo) : 0.f;
+          const float ca = warp_scan(pa, lane);
+          const float cb = warp_scan(pb, lane) + __shfl_sync(kAll, ca, 31);
+          const unsigned ba = __ballot_sync(kAll, r.base + ca >= tz);
+          const unsigned bb = __ballot_sync(kAll, lane + 32 < nc && r.base + cb >= tz);
+          const int q = ba ? __ffs(ba) - 1 : bb ? 32 + __ffs(bb) - 1 : nc - 1;
+          const uint32_t cut = q < 32 ? __shfl_sync(kAll, a, q & 31) : __shfl_sync(kAll, b, q & 31);
+          const uint32_t kd = cut >> 11;
+          K = kd + lo;
+          R = __popc(__ballot_sync(kAll, lane < q && (a >> 11) == kd)) +
+              __popc(__ballot_sync(kAll, lane + 32 < q && (b >> 11) == kd));
+          ties_at_K = __popc(__ballot_sync(kAll, (a >> 11) == kd)) +
+                      __popc(__ballot_sync(kAll, lane + 32 < nc && (b >> 11) == kd));
+        }
+        done = true;
         break;
       }
-      const int top = 31 - __clz(lo ^ (hi - 1u));
-      const int sh = top > 4 ? top - 4 : 0;
-      const uint32_t d0 = lo >> sh;
+      if (r.hi - r.lo == 1u) {
+        finish_ties(r);
+        break;
+      }
+      const int sh = bucket_shift(r);
+      const uint32_t d0 = r.lo >> sh, lo = r.lo, w = r.hi - r.lo;
 #pragma unroll
       for (int b = 0; b < kBuckets; ++b) ws.mass[b][lane] = 0.f;
 #pragma unroll
-      for (int b = 0; b < kBuckets / 4; ++b) ws.count[b][lane] = 0u;
-#pragma unroll
-      for (int m = 0; m < NV; ++m)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t u = __float_as_uint(p[m][e]);
-          if (valid(m, e) && u >= lo && u < hi) {
-            const int b = (int)((u >> sh) - d0);
-            ws.mass[b][lane] += p[m][e];
-            ws.count[b >> 2][lane] += 1u << (8 * (b & 3));
-          }
-        }
-      __syncwarp();
-      // lane b sums bucket b over the lanes (fixed order: deterministic)
-      float bmass = 0.f;
-      int bcount = 0;
-      const int cshift = 8 * (lane & 3);
-#pragma unroll
-      for (int l = 0; l < 32; ++l) {
-        bmass += ws.mass[lane][l];
-        bcount += (int)((ws.count[lane >> 2][l] >> cshift) & 0xffu);
+      for (int b = 0; b < kBuckets / 2; ++b) ws.count[b][lane] = 0u;
+#pragma unroll 1
+      for (int sl = 0; sl < cmax; ++sl) {
+        const uint32_t key = ws.list_key[sl][lane];
+        const bool in = sl < nl && key - lo < w;
+        const uint32_t b = in ? (key >> sh) - d0 : (uint32_t)kBuckets;  // else the sink
+        ws.mass[b][lane] += __uint_as_float(key);
+        ws.count[b >> 1][lane] += 1u << (16 * (b & 1u));
       }
       __syncwarp();
-      const float cum = warp_scan(bmass, lane);
-      const unsigned bal = __ballot_sync(0xffffffffu, base + cum >= t);
-      // The whole row sums to 1 > t; if fp32 rounding leaves the bucket sums just
-      // short of t, the cut falls in the last bucket of the range (the heaviest
-      // block is always kept).
-      const int bs = bal ? __ffs(bal) - 1 : (int)(((hi - 1u) >> sh) - d0);
-      base += __shfl_sync(0xffffffffu, cum - bmass, bs);
-      const int cnt = __shfl_sync(0xffffffffu, bcount, bs);
-      in_range = cnt;
-      lo = max(lo, (d0 + (uint32_t)bs) << sh);
-      hi = min(hi, (d0 + (uint32_t)bs + 1u) << sh);
-      const int wbits = 32 - __clz(hi - lo - 1u);  // bits spanned by the new range
-      if (cnt <= kMaxCand && wbits <= 21) {
-        // ---- exact finish on the bucket's blocks: (key - lo) packs with an
-        // 11-bit block index into 32 bits
-        int nc = 0;
-#pragma unroll
-        for (int m = 0; m < NV; ++m) {
-          uint32_t flags = 0u;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t u = __float_as_uint(p[m][e]);
-            if (valid(m, e) && u >= lo && u < hi) flags |= 1u << e;
-          }
-          const int c = __popc(flags);
-          const int incl_c = warp_scan_i(c, lane);
-          int at = nc + incl_c - c;
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (flags & (1u << e))
-              ws.cand[at++] = ((__float_as_uint(p[m][e]) - lo) << 11) | (uint32_t)(128 * m + 4 * lane + e);
-          nc += __shfl_sync(0xffffffffu, incl_c, 31);
-        }
-        __syncwarp();
-        uint32_t a = lane < nc ? ws.cand[lane] : 0xffffffffu;
-        uint32_t b = lane + 32 < nc ? ws.cand[lane + 32] : 0xffffffffu;
-        __syncwarp();
-        warp_sort64(a, b, lane);
-        // running sums in sorted order: positions lane (a) and lane + 32 (b)
-        const float pa = lane < nc ? __uint_as_float((a >> 11) + lo) : 0.f;
-        const float pb = lane + 32 < nc ? __uint_as_float((b >> 11) + lo) : 0.f;
-        const float ca = warp_scan(pa, lane);
-        const float cb = warp_scan(pb, lane) + __shfl_sync(0xffffffffu, ca, 31);
-        const unsigned ba = __ballot_sync(0xffffffffu, lane < nc && base + ca >= t);
-        const unsigned bb = __ballot_sync(0xffffffffu, lane + 32 < nc && base + cb >= t);
-        int q;  // sorted position of the cut
-        if (ba)
-          q = __ffs(ba) - 1;
-        else if (bb)
-          q = 32 + __ffs(bb) - 1;
-        else
-          q = nc - 1;  // rounding: keep the heaviest candidate
-        const uint32_t cut =
-            q < 32 ? __shfl_sync(0xffffffffu, a, q & 31) : __shfl_sync(0xffffffffu, b, q & 31);
-        const uint32_t kd = cut >> 11;
-        K = kd + lo;
-        // tie rank of the cut among blocks with key K = sorted candidates before it with key K
-        const bool ta = lane < q && (a >> 11) == kd;
-        const bool tb = lane + 32 < q && (b >> 11) == kd;
-        R = __popc(__ballot_sync(0xffffffffu, ta)) + __popc(__ballot_sync(0xffffffffu, tb));
-        const bool ea = lane < nc && (a >> 11) == kd, eb = lane + 32 < nc && (b >> 11) == kd;
-        ties_at_K = __popc(__ballot_sync(0xffffffffu, ea)) + __popc(__ballot_sync(0xffffffffu, eb));
-        break;
-      }
-      if (pass == 6) {  // unreachable for keys of p in (0, 1]; keep a defined result
-        K = lo;
-        R = 0;
-      }
+      const float bmass = column_mass(ws, lane);
+      const int bcount = column_count(ws, lane);
+      __syncwarp();
+      const int bs = choose_bucket(r, bmass, tz, sh, d0, lane);
+      r.n = __shfl_sync(kAll, bcount, bs);
+    }
+    if (!done) {  // unreachable: a < 2^25 key range narrows to one key in 5 list passes
+      K = r.lo;
+      R = 0;
     }
   }
 
-  // ---- emit kept indices in ascending order
+  // ---- keep flags: one nibble per group, bit e = column 128 m + 4 lane + e
   const uint8_t *sta_row = sta + (size_t)i * s1;
-  int32_t *out = kv_inds + row * s1;
-  const bool keep_all = !(t > 0.f);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int count = 0, ties = 0;
+  uint32_t kn[NV];
+  const bool ranked = !keep_all && ties_at_K > 1;  // ties at the cut: rank them (rare)
+  int ties = 0;
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
-    if (!FULL && m >= nv) break;
+    kn[m] = 0u;
+    if (!FULL && m >= nv) continue;
     const int j0 = 128 * m + 4 * lane;
     uint32_t sbits;  // STA flags of the four columns, byte e = column j0 + e
     if (sta_words) {  // s1 % 4 == 0 and a 4-byte aligned STA: one word per lane
@@ -321,76 +434,121 @@ __global__ void __launch_bounds__(kWarps * 32) select_kernel(const float *__rest
       for (int e = 0; e < 4; ++e)
         if (j0 + e < s1) sbits |= (uint32_t)sta_row[j0 + e] << (8 * e);
     }
-    int rank = 0;
-    if (ties_at_K > 1 && !keep_all) {  // rank blocks with key K in index order
+    // nonzero bytes -> bits 0, 8, 16, 24 -> nibble bits 0..3 (the multiply's
+    // partial products land on distinct bits, so nothing carries)
+    sbits |= sbits >> 4;
+    sbits |= sbits >> 2;
+    sbits |= sbits >> 1;
+    const uint32_t sta_nib = ((sbits & 0x01010101u) * 0x00204081u >> 21) & 0xfu;
+    uint32_t keep = 0u;
+    if (!ranked) {
+      const uint32_t Kc = keep_all ? 0u : K;  // keep_all: every key qualifies
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (valid(m, e) && __float_as_uint(p[m][e]) >= Kc) keep |= 1u << e;
+    } else {
       uint32_t tie = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (valid(m, e) && __float_as_uint(p[m][e]) == K) tie |= 1u << e;
-      const int tc = __popc(tie);
-      const int tincl = warp_scan_i(tc, lane);
-      rank = ties + tincl - tc;
-      ties += __shfl_sync(0xffffffffu, tincl, 31);
-    }
-    uint32_t keep = 0u;
+      const uint32_t tc = (uint32_t)__popc(tie);
+      const uint32_t tincl = warp_scan_u(tc, lane);
+      int rank = ties + (int)(tincl - tc);
+      ties += (int)__shfl_sync(kAll, tincl, 31);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (!valid(m, e)) continue;
-      const uint32_t u = __float_as_uint(p[m][e]);
-      bool k;
-      if (keep_all)
-        k = true;
-      else if (u != K)
-        k = u > K;
-      else
-        k = rank++ >= R;
-      if (k || ((sbits >> (8 * e)) & 0xffu) != 0u) keep |= 1u << e;
+      for (int e = 0; e < 4; ++e) {
+        if (!valid(m, e)) continue;
+        const uint32_t u = __float_as_uint(p[m][e]);
+        if (u > K || (u == K && rank++ >= R)) keep |= 1u << e;
+      }
     }
-    const unsigned b0 = __ballot_sync(0xffffffffu, keep & 1u);
-    const unsigned b1 = __ballot_sync(0xffffffffu, keep & 2u);
-    const unsigned b2 = __ballot_sync(0xffffffffu, keep & 4u);
-    const unsigned b3 = __ballot_sync(0xffffffffu, keep & 8u);
-    int at = count + __popc(b0 & lt_mask) + __popc(b1 & lt_mask) + __popc(b2 & lt_mask) +
-             __popc(b3 & lt_mask);
+    uint32_t vmask = 0xfu;
+    if (!FULL) {
+      vmask = 0u;
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (keep & (1u << e)) out[at++] = j0 + e;
-    count += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+      for (int e = 0; e < 4; ++e)
+        if (valid(m, e)) vmask |= 1u << e;
+    }
+    kn[m] = keep | (sta_nib & vmask);
+  }
+  // ---- emit kept indices in ascending order: byte k of the packed scan is
+  // group m0 + k (a group holds at most 128 kept blocks: no carries)
+  int32_t *out = kv_inds + row * s1;
+  int count = 0;
+#pragma unroll
+  for (int m0 = 0; m0 < NV; m0 += 4) {
+    uint32_t wcount = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (m0 + k < NV) wcount |= (uint32_t)__popc(kn[m0 + k]) << (8 * k);
+    const uint32_t incl = warp_scan_u(wcount, lane);
+    const uint32_t total = __shfl_sync(kAll, incl, 31);
+    const uint32_t excl = incl - wcount;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int m = m0 + k;
+      if (m >= NV) break;
+      int at = count + (int)((excl >> (8 * k)) & 0xffu);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kn[m] & (1u << e)) out[at++] = 128 * m + 4 * lane + e;
+      count += (int)((total >> (8 * k)) & 0xffu);
+    }
   }
   if (lane == 0) kv_nb[row] = count;
 }
 
+struct SelectLaunch {
+  dim3 grid;
+  cudaStream_t st;
+  const float *L;
+  long row0, bstride;
+  int nrows, s1;
+  const uint8_t *sta;
+  float t;
+  int32_t *kv_nb, *kv_inds;
+};
+
 template <int NV>
-void launch_nv(unsigned grid, cudaStream_t st, const float *L, long rows, int s1,
-               const uint8_t *sta, float t, int32_t *kv_nb, int32_t *kv_inds) {
-  const bool words = (s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(sta) & 3u) == 0;
-  if (s1 == 128 * NV)
-    select_kernel<NV, true>
-        <<<grid, kWarps * 32, 0, st>>>(L, rows, s1, sta, words, t, kv_nb, kv_inds);
+void launch_nv(const SelectLaunch &a) {
+  const bool words = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sta) & 3u) == 0;
+  if (a.s1 == 128 * NV)
+    select_kernel<NV, true><<<a.grid, kWarps * 32, 0, a.st>>>(
+        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, a.t, a.kv_nb, a.kv_inds);
   else
-    select_kernel<NV, false>
-        <<<grid, kWarps * 32, 0, st>>>(L, rows, s1, sta, words, t, kv_nb, kv_inds);
+    select_kernel<NV, false><<<a.grid, kWarps * 32, 0, a.st>>>(
+        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, a.t, a.kv_nb, a.kv_inds);
 }
 
 }  // namespace
 
-cudaError_t launch_select(const float *L, const Shape &s, const uint8_t *sta, float t,
-                          int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
-  const long rows = (long)s.B * s.h * s.s1;
-  const unsigned grid = (unsigned)((rows + kWarps - 1) / kWarps);
+cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
+                          float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
+  const int nrows = (h1 - h0) * s.s1;
+  SelectLaunch a{dim3((unsigned)((nrows + kWarps - 1) / kWarps), (unsigned)s.B),
+                 st,
+                 L,
+                 (long)h0 * s.s1,
+                 (long)s.h * s.s1,
+                 nrows,
+                 s.s1,
+                 sta,
+                 t,
+                 kv_nb,
+                 kv_inds};
   const int nv = (s.s1 + 127) / 128;
   if (nv <= 1)
-    launch_nv<1>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<1>(a);
   else if (nv <= 2)
-    launch_nv<2>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<2>(a);
   else if (nv <= 4)
-    launch_nv<4>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<4>(a);
   else if (nv <= 8)
-    launch_nv<8>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<8>(a);
   else if (nv <= 12)
-    launch_nv<12>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<12>(a);
   else
-    launch_nv<16>(grid, st, L, rows, s.s1, sta, t, kv_nb, kv_inds);
+    launch_nv<16>(a);
   return cudaGetLastError();
 }
 

@@ -220,6 +220,80 @@ def test_max_blocks_2048(nabla):
     check_attention(nabla, w, data, nb, inds, sample_qblocks(w, 6))
 
 
+def _block_constant(means):
+    """[1, S, h, D] f32 whose every token equals its block's mean; means is [h, s1, D]."""
+    h, s1, D = means.shape
+    x = np.repeat(means.transpose(1, 0, 2)[:, None], 64, axis=1)
+    return np.ascontiguousarray(x.reshape(1, s1 * 64, h, D), dtype=np.float32)
+
+
+def _designed_rows(nabla, b, thr, D=64):
+    """Pooled logits L[head, i, j] = a_i * b[head, j] / sqrt(D), with row scales
+    a_i in {0, 1, 1.5, 2} (a_i = 0: a row of exact ties).  With no STA, the
+    kept set is the CDF part alone; it must equal the oracle's except inside
+    the 1e-4 window around 1 - thr (exact ties are resolved by index on both
+    sides, so no near-tie allowance)."""
+    h, s1 = b.shape
+    a = np.array([0.0, 1.0, 1.5, 2.0], np.float32)[np.arange(s1) % 4]
+    qm = np.zeros((h, s1, D), np.float32)
+    qm[:, :, 0] = a[None, :]
+    km = np.zeros((h, s1, D), np.float32)
+    km[:, :, 0] = b
+    q, k = _block_constant(qm), _block_constant(km)
+    sta = np.zeros((s1, s1), np.uint8)
+    nb, inds = nabla.nabla_build_mask(torch.from_numpy(q).to(DEV), torch.from_numpy(k).to(DEV),
+                                      torch.from_numpy(sta).to(DEV), thr)
+    assert nabla.nabla_get_last_device_status() == 0
+    nb, inds = nb.cpu().numpy(), inds.cpu().numpy()
+    ref = O.build_mask(q.astype(np.float64), k.astype(np.float64), sta, thr)
+    got = csr_to_mask(nb, inds, s1)
+    window = O.ambiguous_blocks(ref["c"], ref["t"], sta, AMB_TOL)
+    bad = (got != ref["mask"]) & ~window
+    assert not bad.any(), f"{int(bad.sum())} mismatches outside the 1e-4 window"
+    assert np.array_equal(nb, got.sum(-1))
+    return got
+
+
+@pytest.mark.parametrize("s1", [1000, 1024])
+@pytest.mark.parametrize("thr", [0.5, 0.9])
+def test_select_clustered_row_overflows_first_bucket(nabla, s1, thr):
+    """Most blocks sit in a 10 % band of probability while two outliers stretch
+    the key range over ~90 binades: the first 32-bucket pass leaves hundreds of
+    blocks in the cut bucket, more than the per-lane list holds, so the row is
+    narrowed again in registers before the list and sort stages."""
+    rng = np.random.default_rng(11)
+    b = np.empty((2, s1), np.float32)
+    for hd in range(2):
+        v = 8.0 * 0.1 * rng.random(s1)           # cluster: L in [0, 0.1)
+        v[-24:] = 8.0 * rng.uniform(-3.0, 0.0, 24)
+        v[0], v[1] = 8.0 * 5.0, -8.0 * 60.0       # heavy and vanishing outliers
+        b[hd] = rng.permutation(v)
+    _designed_rows(nabla, b, thr)
+
+
+@pytest.mark.parametrize("s1", [1000, 1024])
+def test_select_runs_of_exact_ties(nabla, s1):
+    """Four distinct logits, ~s1/4 blocks each: the cut lands inside a run of
+    exact ties that the list passes narrow to a single key."""
+    rng = np.random.default_rng(12)
+    b = (2.0 * rng.integers(0, 4, size=(2, s1))).astype(np.float32)
+    got = _designed_rows(nabla, b, 0.9)
+    # rows with a_i = 0 are all ties: the kept blocks are the highest indices
+    for i in range(0, s1, 4):
+        kept = np.nonzero(got[0, 0, i])[0]
+        assert np.array_equal(kept, np.arange(s1 - kept.size, s1))
+
+
+def test_select_repeated_levels(nabla):
+    """200 distinct levels, each on ~5 blocks: the final candidates hold
+    exact ties, whose tie rank decides which copies of the cut level stay."""
+    rng = np.random.default_rng(13)
+    s1 = 1024
+    b = (8.0 * 3.0 * rng.integers(0, 200, size=(2, s1)) / 200.0).astype(np.float32)
+    for thr in (0.3, 0.7, 0.95):
+        _designed_rows(nabla, b, thr)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_hand_made_csr_edge_rows(nabla, dtype):
     """Empty rows give zero output, single-block rows, full rows, and an
@@ -289,6 +363,51 @@ def test_mask_builder_deterministic(nabla):
     nb = a[0]
     for idx in np.ndindex(nb.shape):
         assert np.array_equal(a[1][idx][:nb[idx]], b[1][idx][:nb[idx]])
+
+
+def _masks_equal(nb_a, inds_a, nb_b, inds_b, s1):
+    a = csr_to_mask(nb_a.cpu().numpy(), inds_a.cpu().numpy(), s1)
+    b = csr_to_mask(nb_b.cpu().numpy(), inds_b.cpu().numpy(), s1)
+    return np.array_equal(a, b)
+
+
+def test_head_group_pipeline_in_cuda_graph_and_side_stream(nabla):
+    """A mask build large enough to run as a head-group pipeline (the select of
+    each group on the library's own stream) gives the same CSR when called on
+    a non-default stream and when captured in a CUDA graph and replayed, and
+    the caller's stream sees the result without any extra synchronisation."""
+    w = W.custom("graph", 1, 16, 128, 64 * 512, (8, 8, 8), sigma=0.75, rho=0.8, thr=(0.9,))
+    data = inputs(w, seed=21)
+    q, k = (nabla.from_storage(data[n], DEV) for n in "qk")
+    sta = nabla.nabla_sta_mask(*w.grid, *w.sta_half_widths, device=DEV)
+    nb0, inds0 = nabla.nabla_build_mask(q, k, sta, 0.9)
+    torch.cuda.synchronize()
+    check_mask(w, 0.9, data, nb0.cpu().numpy(), inds0.cpu().numpy(), sta.cpu().numpy())
+
+    s = torch.cuda.Stream()
+    kv_nb, kv_inds = torch.empty_like(nb0), torch.empty_like(inds0)
+    ws = torch.empty(nabla.nabla_build_mask_workspace_bytes(w.B, w.S, w.h, w.D),
+                     dtype=torch.uint8, device=DEV)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        kv_nb.fill_(-1)
+        nabla.nabla_build_mask(q, k, sta, 0.9, kv_nb, kv_inds, ws, stream=s)
+        copy_nb = kv_nb.clone()  # ordered after the join on s
+    torch.cuda.synchronize()
+    assert torch.equal(copy_nb, nb0)
+    assert _masks_equal(kv_nb, kv_inds, nb0, inds0, w.s1)
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        nabla.nabla_build_mask(q, k, sta, 0.9, kv_nb, kv_inds, ws, stream=s)
+    for _ in range(2):
+        kv_nb.fill_(-1)
+        kv_inds.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(kv_nb, nb0)
+        assert _masks_equal(kv_nb, kv_inds, nb0, inds0, w.s1)
+    assert nabla.nabla_get_last_device_status() == 0
 
 
 def test_bounded_wait_gives_up_and_reports_timeout(nabla):
