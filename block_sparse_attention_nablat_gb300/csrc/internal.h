@@ -36,8 +36,8 @@ struct MaskWorkspace {
 MaskWorkspace mask_workspace_layout(const Shape &s);
 
 // The mask kernels below each cover heads [h0, h1) of every batch.
-// K1: block means of q and k -> tf32 hi at qa/ka, tf32 lo at +lo_off elements,
-// each [B, h, s1, D].
+// K1: block means of q (times log2(e)/sqrt(D)) and k -> tf32 hi at qa/ka, tf32 lo
+// at +lo_off elements, each [B, h, s1, D].
 cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, int h0,
                         int h1, float *qa, float *ka, size_t lo_off, cudaStream_t st);
 // K2a: pooled map in base-2 units, L = qa ka^T log2(e) / sqrt(D), fp32 [B, h, s1, s1],

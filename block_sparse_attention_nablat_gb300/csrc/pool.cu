@@ -11,9 +11,13 @@
 // the four partial sums are combined in shared memory.  Each mean m is written
 // as two tf32 values, hi = m rounded to tf32 and lo = (m - hi) rounded to tf32
 // ([B, h, s1, D] each), the operands of the three-term tf32 pooled-map GEMM.
+// The q means carry the map's scale log2(e)/sqrt(D) (the map is formed in
+// base-2 units), so the GEMM's epilogue stores its accumulators as they are.
 // HBM-bound: the algorithmic traffic is the single read of q and k plus the
 // (small) means.
 #include <cuda_bf16.h>
+
+#include <cmath>
 
 #include "internal.h"
 
@@ -78,7 +82,8 @@ __device__ __forceinline__ float to_tf32(float x) {
 template <typename T>
 __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
                                                    const T *__restrict__ k, int S, int h, int D,
-                                                   int c0, int c1, float *__restrict__ qa,
+                                                   int c0, int c1, float q_scale,
+                                                   float *__restrict__ qa,
                                                    float *__restrict__ ka, size_t lo_off) {
   constexpr int E = Chunk<T>::kElems;
   __shared__ float part[kRowGroups][kChunksPerCta * E];
@@ -115,10 +120,11 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
 
   // 64 chunks * E elements per CTA, spread over the 256 threads.
   float *dst = is_k ? ka : qa;
+  const float mul = is_k ? 1.0f / 64.0f : q_scale * (1.0f / 64.0f);
   for (int e = threadIdx.x; e < kChunksPerCta * E; e += blockDim.x) {
     const int col = cb * E + e;
     if (col >= c1 * E) break;
-    const float m = (part[0][e] + part[1][e] + part[2][e] + part[3][e]) * (1.0f / 64.0f);
+    const float m = (part[0][e] + part[1][e] + part[2][e] + part[3][e]) * mul;
     const int hh = col / D, d = col - hh * D;
     const size_t at = (((size_t)b * h + hh) * s1 + i) * D + d;
     const float hi = to_tf32(m);
@@ -133,15 +139,16 @@ cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shap
                         int h1, float *qa, float *ka, size_t lo_off, cudaStream_t st) {
   const int E = dt == NABLA_BF16 ? 8 : 4;  // D is a multiple of 64: heads start on a chunk
   const int c0 = h0 * s.D / E, c1 = h1 * s.D / E;
+  const float q_scale = (float)(1.4426950408889634 / sqrt((double)s.D));
   dim3 grid(s.s1, (c1 - c0 + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
   if (dt == NABLA_BF16)
     pool_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), s.S, s.h,
-        s.D, c0, c1, qa, ka, lo_off);
+        s.D, c0, c1, q_scale, qa, ka, lo_off);
   else
     pool_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(q),
                                              static_cast<const float *>(k), s.S, s.h, s.D, c0,
-                                             c1, qa, ka, lo_off);
+                                             c1, q_scale, qa, ka, lo_off);
   return cudaGetLastError();
 }
 
