@@ -6,12 +6,19 @@
 // Methodology "Expansion".  The flex-attention kernel the page calls is prior
 // art; this kernel is designed for sm_103a:
 //
-//  * Work unit = (batch, head, pair of adjacent query blocks): 128 query rows,
-//    the M = 128 shape of a single-CTA tcgen05 MMA.  The unit walks the UNION
-//    of the two blocks' kept-KV lists in ascending order; each entry carries
-//    two membership bits, and rows of a block that did not keep an entry get
-//    P = 0 for it.  Persistent CTAs (one per SM) take units round-robin in
-//    head-major order, so co-running CTAs share one head's K/V in L2.
+//  * Work unit = (batch, head, pair of query blocks): 128 query rows, the
+//    M = 128 shape of a single-CTA tcgen05 MMA.  The unit walks the UNION of
+//    the two blocks' kept-KV lists in ascending order; each entry carries two
+//    membership bits, and rows of a block that did not keep an entry get P = 0
+//    for it.  Blocks are paired at a stride d (block i with i + d inside each
+//    run of 2d blocks), and the kernel picks d itself: before starting, every
+//    CTA counts the list unions of the same fixed sample of pairs for each d
+//    with 2d dividing s1 (integer counts, so all CTAs agree) and takes the d
+//    with the fewest.  On a video latent the temporal neighbour (d = H*W)
+//    shares more of its kept list than the horizontal one (d = 1), so fewer
+//    MMAs are spent on entries only one block of the pair needs.  Persistent
+//    CTAs (one per SM) take units round-robin in head-major order, so
+//    co-running CTAs share one head's K/V in L2.
 //  * A step covers two KV entries (128 keys).  On this hardware a tcgen05 MMA
 //    costs about 32 + N/2 cycles whatever its N, so S = Q K^T is issued with
 //    N = 128 (both entries of the step in one MMA, from a K "pair slot" whose
@@ -134,7 +141,15 @@ struct Params {
   int B, S, h;
   float scale_log2;
   int *status;
+  int pstride;  // query blocks i and i + pstride form a pair (set in the kernel)
 };
+
+// Query block `side` (0 or 1) of pair pr at stride d: pairs run through groups
+// of 2d consecutive blocks, (g 2d + o, g 2d + o + d) for o < d.
+__device__ __forceinline__ int pair_block(int pr, int side, int d) {
+  const int g = pr / d;
+  return 2 * g * d + (pr - g * d) + side * d;
+}
 
 struct Unit {
   int b, hh, pr;
@@ -252,7 +267,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     bool bad = false;
 #pragma unroll
     for (int side = 0; side < 2; ++side) {
-      const int qb = 2 * un.pr + side;
+      const int qb = pair_block(un.pr, side, P.pstride);
       if (qb >= s1) break;
       const size_t row = (size_t)bh * s1 + qb;
       int cnt = P.kv_nb[row];
@@ -287,11 +302,13 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
       stop = true;
       continue;
     }
-    mbar_expect_tx(bar.q_full, C::kQBytes);
+    mbar_expect_tx(bar.q_full, C::kQBytes);  // a block past s1 is zero-filled
 #pragma unroll
-    for (int c = 0; c < C::kBoxes; ++c)
-      tma_load_4d(smem + C::kOffQ + c * 128 * 128, tmQ, bar.q_full, c * 64, un.hh, un.pr * 128,
-                  un.b);
+    for (int side = 0; side < 2; ++side)
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_4d(smem + C::kOffQ + c * 128 * 128 + side * 64 * 128, tmQ, bar.q_full, c * 64,
+                    un.hh, pair_block(un.pr, side, P.pstride) * 64, un.b);
     ++kq;
     const int steps = (cnt + 1) >> 1;
     Cursor ck{0, inf.a[0] | inf.b[0]}, cv = ck;
@@ -495,7 +512,7 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
     const int n = live ? info[ub].n : 0;
     const int steps = (n + 1) >> 1;
     const Unit un = decode(u, npairs, P.h);
-    const int qb = 2 * un.pr + half;
+    const int qb = pair_block(un.pr, half, P.pstride);
     float m_run = -INFINITY, l_run = 0.f;
     Cursor cur{0, info[ub].a[0] | info[ub].b[0]};
     for (int s = 0; s < steps; ++s) {
@@ -649,6 +666,83 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
   }
 }
 
+// Pairing stride: the candidate d (1, or any d with 2d dividing s1) whose
+// pairs have the smallest total list union over a fixed sample of pairs.  Run
+// by all 384 threads of every CTA on scratch shared memory before the roles
+// start; integer counts make the choice identical in every CTA.
+constexpr int kMaxCands = 24, kSamples = 16;
+struct StrideScratch {
+  uint32_t bits[12][kMaxWords];
+  unsigned long long total[kMaxCands];
+  int cand[kMaxCands];
+  int ncand, chosen;
+};
+
+__device__ int choose_pair_stride(const Params &P, StrideScratch *sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
+  const long units = (long)P.B * P.h * npairs;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    sc->cand[n++] = 1;
+    for (int d = 2; 2 * d <= s1 && n < kMaxCands; ++d)
+      if (s1 % (2 * d) == 0) sc->cand[n++] = d;
+    sc->ncand = n;
+    for (int c = 0; c < kMaxCands; ++c) sc->total[c] = 0ull;
+  }
+  __syncthreads();
+  const int ncand = sc->ncand;
+  if (ncand > 1) {
+    uint32_t *bits = sc->bits[warp];
+    for (int t = warp; t < ncand * kSamples; t += 12) {
+      const int c = t / kSamples, k = t - c * kSamples;
+      const int d = sc->cand[c];
+      // the same units for every candidate, spread over all heads and rows
+      const long u = (long)(((unsigned long long)k * 2654435761ull) % (unsigned long long)units);
+      const Unit un = decode(u, npairs, P.h);
+      const long bh = (long)un.b * P.h + un.hh;
+      int cnt[2];
+      const int32_t *list[2];
+#pragma unroll
+      for (int side = 0; side < 2; ++side) {
+        const int qb = pair_block(un.pr, side, d);
+        const size_t row = (size_t)bh * s1 + (qb < s1 ? qb : 0);
+        const int n = qb < s1 ? P.kv_nb[row] : 0;
+        cnt[side] = n < 0 ? 0 : (n > s1 ? s1 : n);
+        list[side] = P.kv_inds + row * s1;
+      }
+      for (int w = lane; w < kMaxWords; w += 32) bits[w] = 0u;
+      __syncwarp();
+      for (int n = lane; n < cnt[0]; n += 32) {
+        const int j = list[0][n];
+        if (j >= 0 && j < s1) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
+      __syncwarp();
+      int uni = 0;  // entries of the second list not in the first
+      for (int w = lane; w < kMaxWords; w += 32) uni += __popc(bits[w]);
+      for (int n = lane; n < cnt[1]; n += 32) {
+        const int j = list[1][n];
+        if (j >= 0 && j < s1 && !((bits[j >> 5] >> (j & 31)) & 1u)) ++uni;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) uni += __shfl_xor_sync(0xffffffffu, uni, o);
+      if (lane == 0) atomicAdd(&sc->total[c], (unsigned long long)uni);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = 0;
+    for (int c = 1; c < ncand; ++c)
+      if (sc->total[c] < sc->total[best]) best = c;
+    sc->chosen = sc->cand[best];
+  }
+  __syncthreads();
+  const int d = sc->chosen;
+  __syncthreads();  // the scratch is handed back to the pipeline after this
+  return d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(384, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -710,17 +804,21 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the K / V staging area is free until the producer starts
+  static_assert(sizeof(StrideScratch) <= (size_t)C::kOffInfo - C::kOffK, "stride scratch fits");
+  Params Pp = P;
+  Pp.pstride = choose_pair_stride(P, reinterpret_cast<StrideScratch *>(smem + C::kOffK));
 
   if (warp == 0) {
-    producer<D>(P, &tmQ, &tmK, &tmV, smem, info, bar, abort);
+    producer<D>(Pp, &tmQ, &tmK, &tmV, smem, info, bar, abort);
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<D>(P, smem, info, bar, tmem, abort);
+    if (lane == 0) qk_issuer<D>(Pp, smem, info, bar, tmem, abort);
     __syncwarp();
   } else if (warp == 2) {
-    if (lane == 0) pv_issuer<D>(P, smem, info, bar, tmem, abort);
+    if (lane == 0) pv_issuer<D>(Pp, smem, info, bar, tmem, abort);
     __syncwarp();
   } else if (warp >= 4) {
-    softmax_epilogue<D>(P, info, smem, bar, tmem, abort);
+    softmax_epilogue<D>(Pp, info, smem, bar, tmem, abort);
   }
 
   tc_fence_before();
@@ -756,7 +854,7 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const Shape &s
   auto enc = tensor_map_encoder(&err);
   if (!enc) return err;
   CUtensorMap mq, mk, mv;
-  if (!make_map(enc, &mq, q, s, 128) || !make_map(enc, &mk, k, s, 64) ||
+  if (!make_map(enc, &mq, q, s, 64) || !make_map(enc, &mk, k, s, 64) ||
       !make_map(enc, &mv, v, s, 64))
     return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
@@ -770,7 +868,7 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const Shape &s
   const long units = (long)s.B * s.h * ((s.s1 + 1) / 2);
   const int grid = (int)(units < sms ? units : sms);
   Params p{static_cast<__nv_bfloat16 *>(o), kv_nb, kv_inds, s.B, s.S, s.h,
-           scale * 1.4426950408889634f, status};
+           scale * 1.4426950408889634f, status, 1};
   kern<<<grid, C::kThreads, smem_bytes<D>(), st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
