@@ -34,15 +34,6 @@ bool valid_dtype(nabla_dtype dt) { return dt == NABLA_F32 || dt == NABLA_BF16; }
 
 nabla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NABLA_OK : NABLA_ERR_CUDA; }
 
-// The mask build runs as a pipeline over groups of heads: the pool and pooled
-// map of a group run on the caller's stream, its select on the side stream, so
-// the select of one group (latency-bound) overlaps the pool of the next
-// (HBM-bound).  About six groups; one when the problem is too small to gain.
-int heads_per_group(const Shape &s) {
-  (void)s;
-  return s.h;
-}
-
 }  // namespace
 
 MaskWorkspace mask_workspace_layout(const Shape &s) {
@@ -109,35 +100,9 @@ nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int 
   cudaError_t e;
   int *status = device_status_ptr(&e);
   if (!status) return NABLA_ERR_CUDA;
-  const int G = heads_per_group(s);
-  if (G >= h) {
-    e = launch_pool(q, k, dt, s, 0, h, qa_hi, ka_hi, lo_off, st);
-    if (e == cudaSuccess) e = launch_pooled_map(qa_hi, qa_lo, ka_hi, ka_lo, s, 0, h, L, status, st);
-    if (e == cudaSuccess) e = launch_select(L, s, 0, h, sta, t, kv_nb, kv_inds, st);
-    return from_cuda(e);
-  }
-  side_stream_lock();
-  SideStream side{};
-  e = side_stream(&side);
-  // fork: the side stream starts after everything already queued on the caller's stream
-  if (e == cudaSuccess) e = cudaEventRecord(side.event, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.event, 0);
-  const bool forked = e == cudaSuccess;
-  for (int h0 = 0; h0 < h && e == cudaSuccess; h0 += G) {
-    const int h1 = h0 + G < h ? h0 + G : h;
-    e = launch_pool(q, k, dt, s, h0, h1, qa_hi, ka_hi, lo_off, st);
-    if (e == cudaSuccess)
-      e = launch_pooled_map(qa_hi, qa_lo, ka_hi, ka_lo, s, h0, h1, L, status, st);
-    if (e == cudaSuccess) e = cudaEventRecord(side.event, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side.stream, side.event, 0);
-    if (e == cudaSuccess) e = launch_select(L, s, h0, h1, sta, t, kv_nb, kv_inds, side.stream);
-  }
-  if (forked) {  // join, also after an error, so the caller's stream stays ordered
-    cudaError_t j = cudaEventRecord(side.event, side.stream);
-    if (j == cudaSuccess) j = cudaStreamWaitEvent(st, side.event, 0);
-    if (e == cudaSuccess) e = j;
-  }
-  side_stream_unlock();
+  e = launch_pool(q, k, dt, s, 0, h, qa_hi, ka_hi, lo_off, st);
+  if (e == cudaSuccess) e = launch_pooled_map(qa_hi, qa_lo, ka_hi, ka_lo, s, 0, h, L, status, st);
+  if (e == cudaSuccess) e = launch_select(L, s, 0, h, sta, t, kv_nb, kv_inds, st);
   return from_cuda(e);
 }
 

@@ -35,7 +35,8 @@ struct MaskWorkspace {
 };
 MaskWorkspace mask_workspace_layout(const Shape &s);
 
-// The mask kernels below each cover heads [h0, h1) of every batch.
+// The mask kernels below each cover heads [h0, h1) of every batch (the mask
+// builder passes all heads).
 // K1: block means of q (times log2(e)/sqrt(D)) and k -> tf32 hi at qa/ka, tf32 lo
 // at +lo_off elements, each [B, h, s1, D].
 cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shape &s, int h0,
@@ -49,16 +50,6 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
 cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
                           float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st);
 
-// A high-priority stream of the library's own on the current device, with one
-// event for fork / join, and the lock that keeps one caller's fork-join
-// sequence from interleaving with another's.  Created on first use.
-struct SideStream {
-  cudaStream_t stream;
-  cudaEvent_t event;
-};
-cudaError_t side_stream(SideStream *out);
-void side_stream_lock();
-void side_stream_unlock();
 // K4: STA window.
 cudaError_t launch_sta(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
                        cudaStream_t st);

@@ -371,11 +371,10 @@ def _masks_equal(nb_a, inds_a, nb_b, inds_b, s1):
     return np.array_equal(a, b)
 
 
-def test_head_group_pipeline_in_cuda_graph_and_side_stream(nabla):
-    """A mask build large enough to run as a head-group pipeline (the select of
-    each group on the library's own stream) gives the same CSR when called on
-    a non-default stream and when captured in a CUDA graph and replayed, and
-    the caller's stream sees the result without any extra synchronisation."""
+def test_mask_builder_on_side_stream_and_in_cuda_graph(nabla):
+    """The mask build gives the same CSR when called on a non-default stream
+    (ordered with the caller's other work on that stream, no extra
+    synchronisation) and when captured in a CUDA graph and replayed."""
     w = W.custom("graph", 1, 16, 128, 64 * 512, (8, 8, 8), sigma=0.75, rho=0.8, thr=(0.9,))
     data = inputs(w, seed=21)
     q, k = (nabla.from_storage(data[n], DEV) for n in "qk")
