@@ -36,6 +36,10 @@ sys.path.insert(0, ROOT)
 from block_sparse_attention_nablat_gb300 import workloads as W  # noqa: E402
 
 METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM GB/s"
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of the workload with the current kernels; the capture, its command and the
+# per-kernel split are in profiles/launches_720p_bf16.md.  Workloads not captured: null.
+NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 25.2501e9, "mask": 1.8225e9}}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -151,6 +155,25 @@ def dist_setup(n_gpus: int):
         dist.init_process_group("nccl")
         return rank, world, local, dist
     return 0, 1, 0, None
+
+
+def reduce_over_ranks(dist, device, total_ms: float, kept: float):
+    """Replicas: the job's time is the slowest rank's timed region, its work the
+    kept blocks of every rank.  Returns (max ms, summed kept blocks)."""
+    if dist is None:
+        return total_ms, kept
+    import torch
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    k = torch.tensor([float(kept)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(k, op=dist.ReduceOp.SUM)
+    return t.item(), k.item()
+
+
+def whole_job_tflops(w, kept_all: float, total_ms: float, steps: int) -> float:
+    """Kept-block attention TFLOP/s of the whole job over the timed steps."""
+    return attn_flops(w, kept_all) / (total_ms / steps * 1e-3) / 1e12
 
 
 def oracle_sample(w, data, sta, thr, kv_nb=None, kv_inds=None, n_qblocks=8, seed=0):
@@ -270,15 +293,9 @@ def run_ours(args, w, thr):
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     assert nabla.nabla_get_last_device_status() == 0
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    kept_t = torch.tensor([float(kept)], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dist.all_reduce(kept_t, op=dist.ReduceOp.SUM)
-    total_ms = t.item()
-    kept_all = kept_t.item()
+    total_ms, kept_all = reduce_over_ranks(dist, dev, total_ms, kept)
     ms_per_step = total_ms / args.steps
-    value = attn_flops(w, kept_all) / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(w, kept_all, total_ms, args.steps)
 
     # end to end through the public API: pinned host q/k/v in, o out, every step
     e2e = None
@@ -349,11 +366,13 @@ def run_ours(args, w, thr):
                   "attn_tflops_dense_equiv": dense_flops(w) / (attn_ms * 1e-3) / 1e12},
         "roofline": {"bound": "tensor", "kernel": "attention forward", "achieved": attn_tflops,
                      "peak": peak_t, "unit": "TFLOP/s", "frac": attn_tflops / peak_t,
-                     "traffic": None, "peak_source": f"{src} bf16 sustained"},
+                     "traffic": NCU_TRAFFIC_BYTES.get(w.name, {}).get("attention"),
+                     "peak_source": f"{src} bf16 sustained"},
         "mask_roofline": {"bound": "hbm", "kernel": "mask build (pool + map + select)",
                           "achieved": mask_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": mask_gbs / peaks["hbm_gbs"], "frac_of_8000": mask_gbs / 8000.0,
-                          "traffic": None, "peak_source": f"{src} hbm"},
+                          "traffic": NCU_TRAFFIC_BYTES.get(w.name, {}).get("mask"),
+                          "peak_source": f"{src} hbm"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * 4,
