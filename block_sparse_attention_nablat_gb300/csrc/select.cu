@@ -81,11 +81,14 @@ __device__ __forceinline__ float exp2_approx(float x) {
 struct WarpScratch {
   float mass[kBuckets + 1][32];          // [bucket][lane]: lane-private columns; last row: sink
   uint32_t count[kBuckets / 2 + 1][32];  // 16-bit fields: bucket 2w (low), 2w + 1 (high)
-  uint32_t list_key[kSlots + 1][32];     // [slot][lane]; last row: sink
-  uint16_t list_idx[kSlots + 1][32];     // block index of the entry (separate array: a 64-bit
-                                         // store would tie every key register to a pair)
+  // [slot][lane]: ((key - list_lo) << 6) | (4 m + e), the entry's key relative to the
+  // bucket it was copied from (< 2^26) and its register position; last row: spill
+  uint32_t list[kSlots + 1][32];
   uint32_t cand[kMaxCand];
 };
+constexpr int kMaxRow = 2048;
+// after the cut is known the scratch holds the row's kept indices for the store
+static_assert(sizeof(WarpScratch) >= kMaxRow * sizeof(int32_t), "row staging fits the scratch");
 
 // The cut range [lo, hi) of keys, the mass below it, and how many blocks it holds.
 struct Range {
@@ -175,8 +178,11 @@ __device__ __forceinline__ void register_pass(WarpScratch &ws, const float (&p)[
 }
 
 // Copy the blocks with keys in [r.lo, r.hi) into this lane's list and return
-// how many there are; past kSlots - 1 they overwrite the last slot (overflow,
-// detected by the caller), and the others write the sink row.
+// how many there are.  Every element writes slot min(c, kSlots) and only an
+// in-range one advances c, so slots [0, c) hold exactly the range's blocks (a
+// later block overwrites an out-of-range write); c > kSlots means overflow,
+// detected by the caller.  The range spans < 2^26 keys (a bucket of a range
+// of keys of e in [0, 1]).
 template <int NV, bool FULL>
 __device__ __forceinline__ int compact_range(WarpScratch &ws, const float (&p)[NV][4],
                                              const Range &r, int lane, int nv, int s1) {
@@ -186,15 +192,17 @@ __device__ __forceinline__ int compact_range(WarpScratch &ws, const float (&p)[N
   for (int m = 0; m < NV; ++m)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t u = __float_as_uint(p[m][e]);
-      const int j = 128 * m + 4 * lane + e;
-      const bool in = (FULL || (m < nv && j < s1)) && u - lo < w;
-      const int slot = in ? min(c, kSlots - 1) : kSlots;
-      ws.list_key[slot][lane] = u;
-      ws.list_idx[slot][lane] = (uint16_t)j;
+      const uint32_t d = __float_as_uint(p[m][e]) - lo;
+      const bool in = (FULL || (m < nv && 128 * m + 4 * lane + e < s1)) && d < w;
+      ws.list[min(c, kSlots)][lane] = (d << 6) | (uint32_t)(4 * m + e);
       c += in ? 1 : 0;
     }
   return c;
+}
+
+// block index of a list entry of this lane
+__device__ __forceinline__ uint32_t entry_index(uint32_t word, int lane) {
+  return 128u * ((word & 63u) >> 2) + 4u * (uint32_t)lane + (word & 3u);
 }
 
 // NV = float4 groups per lane (s1 <= 128 * NV); FULL: s1 == 128 * NV exactly,
@@ -204,9 +212,9 @@ __device__ __forceinline__ int compact_range(WarpScratch &ws, const float (&p)[N
 template <int NV, bool FULL>
 __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     select_kernel(const float *__restrict__ L, long row0, long bstride, int nrows, int s1,
-                  const uint8_t *__restrict__ sta, bool sta_words, float t,
+                  const uint8_t *__restrict__ sta, bool sta_words, bool vec_out, float t,
                   int32_t *__restrict__ kv_nb, int32_t *__restrict__ kv_inds) {
-  __shared__ WarpScratch scratch[kWarps];
+  __shared__ __align__(16) WarpScratch scratch[kWarps];  // 16-byte reads and writes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int local = blockIdx.x * kWarps + warp;
   if (local >= nrows) return;  // uniform per warp
@@ -282,11 +290,13 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
       done = true;
     };
     int c = 0;  // this lane's list entries (more than kSlots: overflow)
+    uint32_t list_lo = 0u;  // key offset of the list entries
     if (r.hi - r.lo == 1u) {
       finish_ties(r);
     } else {
       register_pass<NV, FULL, false>(ws, p, r, tz, lane, nv, s1);
       c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
+      list_lo = r.lo;
       r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
       // rare: the cut bucket overflows a lane's list; narrow it in registers
 #pragma unroll 1
@@ -300,6 +310,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
         } else {
           register_pass<NV, FULL, true>(ws, p, r, tz, lane, nv, s1);
           c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
+          list_lo = r.lo;
           r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
         }
       }
@@ -315,11 +326,12 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
         int nc = 0;
 #pragma unroll 1
         for (int sl = 0; sl < cmax; ++sl) {
-          const uint32_t key = ws.list_key[sl][lane];
+          const uint32_t word = ws.list[sl][lane];
+          const uint32_t key = list_lo + (word >> 6);
           const bool in = sl < nl && key - lo < w;
           const unsigned bal = __ballot_sync(kAll, in);
           const int at = nc + __popc(bal & lt_mask);
-          if (in && at < kMaxCand) ws.cand[at] = ((key - lo) << 11) | ws.list_idx[sl][lane];
+          if (in && at < kMaxCand) ws.cand[at] = ((key - lo) << 11) | entry_index(word, lane);
           nc += __popc(bal);
         }
         nc = min(nc, kMaxCand);
@@ -396,7 +408,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
       for (int b = 0; b < kBuckets / 2; ++b) ws.count[b][lane] = 0u;
 #pragma unroll 1
       for (int sl = 0; sl < cmax; ++sl) {
-        const uint32_t key = ws.list_key[sl][lane];
+        const uint32_t key = list_lo + (ws.list[sl][lane] >> 6);
         const bool in = sl < nl && key - lo < w;
         const uint32_t b = in ? (key >> sh) - d0 : (uint32_t)kBuckets;  // else the sink
         ws.mass[b][lane] += __uint_as_float(key);
@@ -472,8 +484,10 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     kn[m] = keep | (sta_nib & vmask);
   }
   // ---- emit kept indices in ascending order: byte k of the packed scan is
-  // group m0 + k (a group holds at most 128 kept blocks: no carries)
-  int32_t *out = kv_inds + row * s1;
+  // group m0 + k (a group holds at most 128 kept blocks: no carries).  They are
+  // staged in the warp's scratch (free now) and then stored row-contiguously.
+  int32_t *stage = reinterpret_cast<int32_t *>(&ws);
+  __syncwarp();  // every lane is done with the scratch's histogram / list contents
   int count = 0;
 #pragma unroll
   for (int m0 = 0; m0 < NV; m0 += 4) {
@@ -491,9 +505,19 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
       int at = count + (int)((excl >> (8 * k)) & 0xffu);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (kn[m] & (1u << e)) out[at++] = 128 * m + 4 * lane + e;
+        if (kn[m] & (1u << e)) stage[at++] = 128 * m + 4 * lane + e;
       count += (int)((total >> (8 * k)) & 0xffu);
     }
+  }
+  __syncwarp();
+  int32_t *out = kv_inds + row * s1;
+  if (vec_out) {  // rows start 16-byte aligned: four indices per lane per store
+    int i = 4 * lane;
+    for (; i + 4 <= count; i += 128)
+      *reinterpret_cast<int4 *>(out + i) = *reinterpret_cast<const int4 *>(stage + i);
+    for (; i < count; ++i) out[i] = stage[i];  // this lane's part of the tail
+  } else {
+    for (int i = lane; i < count; i += 32) out[i] = stage[i];
   }
   if (lane == 0) kv_nb[row] = count;
 }
@@ -512,12 +536,13 @@ struct SelectLaunch {
 template <int NV>
 void launch_nv(const SelectLaunch &a) {
   const bool words = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sta) & 3u) == 0;
+  const bool vec = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.kv_inds) & 15u) == 0;
   if (a.s1 == 128 * NV)
     select_kernel<NV, true><<<a.grid, kWarps * 32, 0, a.st>>>(
-        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, a.t, a.kv_nb, a.kv_inds);
+        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
   else
     select_kernel<NV, false><<<a.grid, kWarps * 32, 0, a.st>>>(
-        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, a.t, a.kv_nb, a.kv_inds);
+        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
 }
 
 }  // namespace
