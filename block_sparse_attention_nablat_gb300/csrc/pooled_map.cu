@@ -22,14 +22,13 @@
 // kind::tf32 MMAs (lo*hi, hi*lo, hi*hi) accumulate a 128 x 128 fp32 tile in
 // TMEM; two accumulators let the epilogue of one tile overlap the MMAs of the
 // next.  TMEM columns: A_hi [0, 128), A_lo [128, 256), accumulators [256, 384)
-// and [384, 512).  Warp roles: 0 = TMA producer, 1 = MMA issuer, 4-7 and 12-15 =
-// epilogue, two 32-column pieces of each tile per warp
+// and [384, 512).  Warp roles: 0 = TMA producer, 1 = MMA issuer, 4-7 = epilogue
 // (the q means already carry log2(e)/sqrt(D) -- the map is kept in base-2
 // units, so the softmax that follows is a plain 2^x -- so the accumulators are
 // stored as they are: 32 x 32 pieces written 128-byte-swizzled to shared memory
-// and sent out by TMA stores, which also clip the ragged edges), 8-11 = strip
-// loaders (A into TMEM for the next strip as soon as the MMAs of the current
-// one are done).  Operand
+// and sent out by TMA stores, which also clip the ragged edges), 8-15 = strip
+// loaders (hi and lo of the next strip into TMEM as soon as the MMAs of the
+// current one are done, its first columns fetched ahead).  Operand
 // tensors are 3-D (D, s1, B*h) so a tile never reads across a head boundary
 // (out-of-range rows are zero-filled and their results are not stored).
 #include <cuda.h>
@@ -49,7 +48,7 @@ constexpr int kStages = 4;
 constexpr int kBBytes = kBN * kBK * 4;    // one 32-column chunk of B (16 KB)
 constexpr int kStageBytes = 2 * kBBytes;  // B_hi, B_lo
 constexpr int kThreads = 512;
-constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, two 32-column pieces each per tile
+constexpr int kEpiWarps = 4;  // one per TMEM lane quarter, four 32-column pieces each per tile
 constexpr uint32_t kColAhi = 0, kColAlo = 128, kColAcc = 256;
 
 // kind::tf32 instruction descriptor: fp32 accumulator (bits 4-5 = 1), A and B
@@ -156,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sync->acc_full[i], 1);
       mbar_init(&sync->acc_empty[i], 32 * kEpiWarps);
     }
-    mbar_init(&sync->a_full, 128);
+    mbar_init(&sync->a_full, 256);
     mbar_init(&sync->a_empty, 1);
     mbar_init(&sync->drain, 1);
     sync->abort = 0;
@@ -228,42 +227,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_commit(&sync->drain);
     mbar_wait(&sync->drain, 0, nullptr, P.status, kDevTimeout);
-  } else if (warp >= 8 && warp < 12) {
-    // ---- strip loader: thread = TMEM lane = strip row; hi and lo rows into TMEM
+  } else if (warp >= 8) {
+    // ---- strip loaders: warps 8-11 write the hi rows, 12-15 the lo rows of the
+    // next strip into TMEM (thread = TMEM lane = strip row).  The first 64
+    // columns are fetched before the wait for the current strip's MMAs, so only
+    // the rest of the row is on the critical path.
     const int q4 = warp & 3;
+    const int part = (warp >> 2) & 1;  // 0: hi, 1: lo
     const int r = q4 * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t col0 = part ? kColAlo : kColAhi;
+    auto fetch = [&](const float *src, int row, int c, uint32_t (&v)[2][32]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (row < P.s1) f = *reinterpret_cast<const float4 *>(src + c + 32 * h + 4 * i);
+          v[h][4 * i] = __float_as_uint(f.x);
+          v[h][4 * i + 1] = __float_as_uint(f.y);
+          v[h][4 * i + 2] = __float_as_uint(f.z);
+          v[h][4 * i + 3] = __float_as_uint(f.w);
+        }
+    };
     uint32_t ls = 0;
     for (long s = blockIdx.x; s < strips && !*abort; s += gridDim.x, ++ls) {
       const int bh = pair_index(P, (int)(s / P.mt));
       const int row = (int)(s % P.mt) * kBM + r;
+      const float *src = (part ? P.qa_lo : P.qa_hi) + ((size_t)bh * P.s1 + row) * P.D;
+      uint32_t v[2][32];
+      fetch(src, row, 0, v);  // in flight while the previous strip finishes
       if (ls > 0) {
         const bool ok = __all_sync(0xffffffffu, mbar_wait(&sync->a_empty, (ls - 1) & 1u, abort,
                                                           P.status, kDevTimeout));
         if (!ok) break;
         tc_fence_after();
       }
+      tmem_st32(tmem + lane_base + col0, v[0]);
+      tmem_st32(tmem + lane_base + col0 + 32, v[1]);
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const float *src = (half ? P.qa_lo : P.qa_hi) + ((size_t)bh * P.s1 + row) * P.D;
-        const uint32_t col0 = half ? kColAlo : kColAhi;
-#pragma unroll 1
-        for (int c = 0; c < P.D; c += 64) {  // 64 columns = 16 loads in flight per thread
-          uint32_t v[2][32];
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (row < P.s1) f = *reinterpret_cast<const float4 *>(src + c + 32 * h + 4 * i);
-              v[h][4 * i] = __float_as_uint(f.x);
-              v[h][4 * i + 1] = __float_as_uint(f.y);
-              v[h][4 * i + 2] = __float_as_uint(f.z);
-              v[h][4 * i + 3] = __float_as_uint(f.w);
-            }
-          tmem_st32(tmem + lane_base + col0 + (uint32_t)c, v[0]);
-          tmem_st32(tmem + lane_base + col0 + (uint32_t)c + 32, v[1]);
-        }
+      for (int c = 64; c < P.D; c += 64) {
+        fetch(src, row, c, v);
+        tmem_st32(tmem + lane_base + col0 + (uint32_t)c, v[0]);
+        tmem_st32(tmem + lane_base + col0 + (uint32_t)c + 32, v[1]);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -271,13 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ---- epilogue: thread = accumulator lane = tile row; warp w owns rows
-    // 32 (w % 4) .. + 31 and the two 32-column pieces 2 (w / 12) .. + 1 of a tile
+    // 32 (w % 4) .. + 31 and writes them in four 32 x 32 pieces per tile
     const int q4 = warp & 3;
-    const int ew = (warp >> 3) * 4 + q4;  // epilogue warp index 0..7
-    const int piece0 = 2 * (warp / 12);
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    uint8_t *wbuf = epi + ew * 2 * kPieceBytes;
-    float *tw = reinterpret_cast<float *>(epi) + ew * 32 * kStagePad;
+    uint8_t *wbuf = epi + q4 * 2 * kPieceBytes;
+    float *tw = reinterpret_cast<float *>(epi) + q4 * 32 * kStagePad;
     uint32_t tc = 0, pc = 0;
     for (long s = blockIdx.x; s < strips && !*abort; s += gridDim.x) {
       const int bh = pair_index(P, (int)(s / P.mt));
@@ -288,45 +292,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           abort, P.status, kDevTimeout));
         if (!ok) break;
         tc_fence_after();
-        uint32_t v[2][32];
-        tmem_ld32(tmem + lane_base + kColAcc + ab * kBN + piece0 * 32, v[0]);
-        tmem_ld32(tmem + lane_base + kColAcc + ab * kBN + piece0 * 32 + 32, v[1]);
-        tmem_wait_ld();
-        reg_fence(v[0]);
-        reg_fence(v[1]);
-        tc_fence_before();
-        mbar_arrive(&sync->acc_empty[ab]);  // this warp's part of the accumulator is in registers
+#pragma unroll 1
+        for (int pair = 0; pair < kBN / 64; ++pair) {
+          uint32_t v[2][32];
+          tmem_ld32(tmem + lane_base + kColAcc + ab * kBN + pair * 64, v[0]);
+          tmem_ld32(tmem + lane_base + kColAcc + ab * kBN + pair * 64 + 32, v[1]);
+          tmem_wait_ld();
+          reg_fence(v[0]);
+          reg_fence(v[1]);
+          if (pair == kBN / 64 - 1) {  // the whole accumulator is in registers: release it
+            tc_fence_before();
+            mbar_arrive(&sync->acc_empty[ab]);
+          }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int col0 = nt * kBN + (piece0 + h) * 32;
-          if (kTma) {
-            // 128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r & 7)
-            uint8_t *buf = wbuf + (pc & 1u) * kPieceBytes;
-            if (lane == 0) bulk_wait_read_1();  // the store of two pieces ago has read buf
-            __syncwarp();
+          for (int h = 0; h < 2; ++h) {
+            const int col0 = nt * kBN + pair * 64 + h * 32;
+            if (kTma) {
+              // 128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r & 7)
+              uint8_t *buf = wbuf + (pc & 1u) * kPieceBytes;
+              if (lane == 0) bulk_wait_read_1();  // the store of two pieces ago has read buf
+              __syncwarp();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              *reinterpret_cast<uint4 *>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                  make_uint4(v[h][4 * k], v[h][4 * k + 1], v[h][4 * k + 2], v[h][4 * k + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && row0 < P.s1 && col0 < P.s1) {
-              tma_store_3d(&tL, buf, col0, row0, bh);
-              bulk_commit();
-            }
-            ++pc;
-          } else {
+              for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4 *>(buf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                    make_uint4(v[h][4 * k], v[h][4 * k + 1], v[h][4 * k + 2], v[h][4 * k + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0 && row0 < P.s1 && col0 < P.s1) {
+                tma_store_3d(&tL, buf, col0, row0, bh);
+                bulk_commit();
+              }
+              ++pc;
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) tw[lane * kStagePad + i] = __uint_as_float(v[h][i]);
-            __syncwarp();
-            const int col = col0 + lane;
-            if (col < P.s1) {
-              float *out = P.L + ((size_t)bh * P.s1 + row0) * P.s1 + col;
+              for (int i = 0; i < 32; ++i) tw[lane * kStagePad + i] = __uint_as_float(v[h][i]);
+              __syncwarp();
+              const int col = col0 + lane;
+              if (col < P.s1) {
+                float *out = P.L + ((size_t)bh * P.s1 + row0) * P.s1 + col;
 #pragma unroll 4
-              for (int rr = 0; rr < 32; ++rr)
-                if (row0 + rr < P.s1) out[(size_t)rr * P.s1] = tw[rr * kStagePad + lane];
+                for (int rr = 0; rr < 32; ++rr)
+                  if (row0 + rr < P.s1) out[(size_t)rr * P.s1] = tw[rr * kStagePad + lane];
+              }
+              __syncwarp();
             }
-            __syncwarp();
           }
         }
       }
