@@ -28,10 +28,11 @@
 //    of step s-1, which is already queued ahead of PV(s), so the tensor pipe
 //    never drains between steps.
 //  * Warp roles: warp 0 builds the unit's entry bitmaps from kv_inds and issues
-//    TMA loads (Q once per unit; K pair slots one step ahead of the per-entry
-//    V tiles); one thread of warp 1 issues every QK^T and one thread of warp 2
-//    every PV (two issue streams, so one stream's waits never leave the tensor
-//    pipe without queued work); warps 4-7 and 8-11 are two
+//    the TMA loads of Q (once per unit) and of the K pair slots, warp 3 those of
+//    the per-entry V tiles (two producers, so a wait for a V slot never holds
+//    back the next K pair); one thread of warp 1 issues every QK^T and one
+//    thread of warp 2 every PV (two issue streams, so one stream's waits never
+//    leave the tensor pipe without queued work); warps 4-7 and 8-11 are two
 //    softmax groups splitting each step's columns (group x takes entry x).
 //    Thread r of a group = TMEM lane r = query row r; the two threads of a row
 //    exchange their partial row max through shared memory every step (a
@@ -235,7 +236,9 @@ __device__ void drain_copies(const Params &P, const Bars &bar, uint32_t gk, uint
   if (kq > 0) mbar_wait(bar.q_full, (kq - 1) & 1u, nullptr, P.status, kDevTimeout);
 }
 
-// Warp 0: entry bitmaps + TMA loads (Q per unit; K pair slots one step ahead of V).
+// Warp 0: entry bitmaps + TMA loads of Q (once per unit) and of the K pair slots,
+// as far ahead as the K ring allows; warp 3 loads the V tiles (v_producer), so a
+// wait for a V slot never holds back the next K pair.
 template <int D>
 __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensorMap *tmK,
                          const CUtensorMap *tmV, uint8_t *smem, UnitInfo *info, const Bars &bar,
@@ -244,7 +247,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
   const int lane = threadIdx.x & 31;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1, words = (s1 + 31) >> 5;
   const long units = (long)P.B * P.h * npairs;
-  uint32_t gk = 0, ge = 0, kq = 0;  // K pair slots issued, V tiles issued, Q tiles issued
+  uint32_t gk = 0, ge = 0, kq = 0;  // K pair slots issued, (V: none here), Q tiles issued
   bool stop = false;  // lane 0: a wait gave up; every lane leaves together at the loop top
   int k = 0;
   for (long u = blockIdx.x; u < units; u += gridDim.x, ++k) {
@@ -311,7 +314,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
                     un.hh, pair_block(un.pr, side, P.pstride) * 64, un.b);
     ++kq;
     const int steps = (cnt + 1) >> 1;
-    Cursor ck{0, inf.a[0] | inf.b[0]}, cv = ck;
+    Cursor ck{0, inf.a[0] | inf.b[0]};
     bool go = true;
     auto load_k = [&](int s) {  // both entries of step s into one pair slot
       const uint32_t ks = gk % C::kKStages;
@@ -331,11 +334,40 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
       }
       ++gk;
     };
-    auto load_v = [&]() {  // next entry's V tile
+    for (int s = 0; s < steps && go; ++s) {
+      load_k(s);
+      if (*abort) go = false;
+    }
+    if (!go) stop = true;
+  }
+  if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, ge, kq);
+}
+
+// Warp 3, lane 0: the V tile of every entry, in entry order, into the V ring.
+template <int D>
+__device__ void v_producer(const Params &P, const CUtensorMap *tmV, uint8_t *smem,
+                           UnitInfo *info, const Bars &bar, volatile int *abort) {
+  using C = Cfg<D>;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
+  const long units = (long)P.B * P.h * npairs;
+  uint32_t ge = 0;
+  bool go = true;
+  int k = 0;
+  for (long u = blockIdx.x; u < units && go && !*abort; u += gridDim.x, ++k) {
+    const int ub = k & 1;
+    if (!mbar_wait(&bar.info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) {
+      go = false;
+      break;
+    }
+    const UnitInfo &inf = info[ub];
+    const int n = inf.n;
+    const Unit un = decode(u, npairs, P.h);
+    Cursor cv{0, inf.a[0] | inf.b[0]};
+    for (int e = 0; e < n && go; ++e) {
       const uint32_t vs = ge % C::kVStages;
-      go = go && mbar_wait(&bar.v_empty[vs], ((ge / C::kVStages) & 1) ^ 1, abort, P.status,
-                           kDevTimeout);
-      if (!go) return;
+      go = mbar_wait(&bar.v_empty[vs], ((ge / C::kVStages) & 1) ^ 1, abort, P.status,
+                     kDevTimeout);
+      if (!go) break;
       uint32_t fl;
       const int j = next_entry(inf, cv, fl);
       mbar_expect_tx(&bar.v_full[vs], C::kTileBytes);
@@ -344,17 +376,14 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
         tma_load_4d(smem + C::kOffV + vs * C::kTileBytes + c * 64 * 128, tmV, &bar.v_full[vs],
                     c * 64, un.hh, j * 64, un.b);
       ++ge;
-    };
-    load_k(0);
-    for (int s = 0; s < steps && go; ++s) {
-      if (s + 1 < steps) load_k(s + 1);
-      load_v();
-      if (2 * s + 1 < cnt) load_v();
-      if (*abort) go = false;
     }
-    if (!go) stop = true;
+    if (!go) break;
+    mbar_arrive(&bar.info_empty[ub]);
   }
-  if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, ge, kq);
+  if (!go || *abort)  // let in-flight copies land before the CTA exits
+    for (uint32_t e = ge > (uint32_t)C::kVStages ? ge - C::kVStages : 0u; e < ge; ++e)
+      mbar_wait(&bar.v_full[e % C::kVStages], (e / C::kVStages) & 1u, nullptr, P.status,
+                kDevTimeout);
 }
 
 // Ring position: slot index and phase parity advanced without division.
@@ -784,7 +813,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.info_full[i], 1);
-      mbar_init(&bar.info_empty[i], 256 + 2);  // softmax threads + both MMA issuers
+      mbar_init(&bar.info_empty[i], 256 + 3);  // softmax threads, both MMA issuers, V loader
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bar.s_full[i], 1);
@@ -816,6 +845,9 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (warp == 2) {
     if (lane == 0) pv_issuer<D>(Pp, smem, info, bar, tmem, abort);
+    __syncwarp();
+  } else if (warp == 3) {
+    if (lane == 0) v_producer<D>(Pp, &tmV, smem, info, bar, abort);
     __syncwarp();
   } else if (warp >= 4) {
     softmax_epilogue<D>(Pp, info, smem, bar, tmem, abort);
