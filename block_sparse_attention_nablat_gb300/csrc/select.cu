@@ -226,6 +226,16 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
   auto valid = [&](int m, int e) { return FULL || (m < nv && 128 * m + 4 * lane + e < s1); };
   const unsigned lt_mask = (1u << lane) - 1u;
 
+  // STA words of this lane's columns (byte e of word m = column 128 m + 4 lane + e),
+  // issued first: consumed only at the end, their latency hides behind the row's work
+  const uint8_t *sta_row = sta + (size_t)i * s1;
+  uint32_t sw[NV];
+#pragma unroll
+  for (int m = 0; m < NV; ++m) {
+    const int j0 = 128 * m + 4 * lane;
+    sw[m] = (sta_words && (FULL || j0 < s1)) ? *reinterpret_cast<const uint32_t *>(sta_row + j0)
+                                              : 0u;
+  }
   // ---- load the row; column of element e of group m is 128 m + 4 lane + e
   float p[NV][4];
 #pragma unroll
@@ -428,7 +438,6 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
   }
 
   // ---- keep flags: one nibble per group, bit e = column 128 m + 4 lane + e
-  const uint8_t *sta_row = sta + (size_t)i * s1;
   uint32_t kn[NV];
   const bool ranked = !keep_all && ties_at_K > 1;  // ties at the cut: rank them (rare)
   int ties = 0;
@@ -438,8 +447,8 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     if (!FULL && m >= nv) continue;
     const int j0 = 128 * m + 4 * lane;
     uint32_t sbits;  // STA flags of the four columns, byte e = column j0 + e
-    if (sta_words) {  // s1 % 4 == 0 and a 4-byte aligned STA: one word per lane
-      sbits = (FULL || j0 < s1) ? *reinterpret_cast<const uint32_t *>(sta_row + j0) : 0u;
+    if (sta_words) {  // s1 % 4 == 0 and a 4-byte aligned STA: loaded at the start
+      sbits = sw[m];
     } else {
       sbits = 0u;
 #pragma unroll
