@@ -440,34 +440,41 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
   // ---- keep flags: one nibble per group, bit e = column 128 m + 4 lane + e
   uint32_t kn[NV];
   const bool ranked = !keep_all && ties_at_K > 1;  // ties at the cut: rank them (rare)
-  int ties = 0;
-#pragma unroll
-  for (int m = 0; m < NV; ++m) {
-    kn[m] = 0u;
-    if (!FULL && m >= nv) continue;
+  auto sta_nibble = [&](int m) -> uint32_t {
     const int j0 = 128 * m + 4 * lane;
-    uint32_t sbits;  // STA flags of the four columns, byte e = column j0 + e
-    if (sta_words) {  // s1 % 4 == 0 and a 4-byte aligned STA: loaded at the start
-      sbits = sw[m];
-    } else {
-      sbits = 0u;
+    uint32_t x = sw[m];  // STA flags of the four columns, byte e = column j0 + e
+    if (!sta_words) {
+      x = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (j0 + e < s1) sbits |= (uint32_t)sta_row[j0 + e] << (8 * e);
+        if (j0 + e < s1) x |= (uint32_t)sta_row[j0 + e] << (8 * e);
     }
     // nonzero bytes -> bits 0, 8, 16, 24 -> nibble bits 0..3 (the multiply's
     // partial products land on distinct bits, so nothing carries)
-    sbits |= sbits >> 4;
-    sbits |= sbits >> 2;
-    sbits |= sbits >> 1;
-    const uint32_t sta_nib = ((sbits & 0x01010101u) * 0x00204081u >> 21) & 0xfu;
-    uint32_t keep = 0u;
-    if (!ranked) {
-      const uint32_t Kc = keep_all ? 0u : K;  // keep_all: every key qualifies
+    x |= x >> 4;
+    x |= x >> 2;
+    x |= x >> 1;
+    return ((x & 0x01010101u) * 0x00204081u >> 21) & 0xfu;
+  };
+  auto valid_nibble = [&](int m) -> uint32_t {
+    uint32_t v = 0u;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (valid(m, e) && __float_as_uint(p[m][e]) >= Kc) keep |= 1u << e;
-    } else {
+    for (int e = 0; e < 4; ++e) v |= (uint32_t)valid(m, e) << e;
+    return v;
+  };
+  if (!ranked) {
+    const uint32_t Kc = keep_all ? 0u : K;  // keep_all: every key qualifies
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
+      uint32_t keep = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) keep |= (uint32_t)(__float_as_uint(p[m][e]) >= Kc) << e;
+      kn[m] = (keep | sta_nibble(m)) & valid_nibble(m);
+    }
+  } else {
+    int ties = 0;
+#pragma unroll
+    for (int m = 0; m < NV; ++m) {
       uint32_t tie = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e)
@@ -476,21 +483,14 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
       const uint32_t tincl = warp_scan_u(tc, lane);
       int rank = ties + (int)(tincl - tc);
       ties += (int)__shfl_sync(kAll, tincl, 31);
+      uint32_t keep = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        if (!valid(m, e)) continue;
         const uint32_t u = __float_as_uint(p[m][e]);
-        if (u > K || (u == K && rank++ >= R)) keep |= 1u << e;
+        if (u > K || (u == K && valid(m, e) && rank++ >= R)) keep |= 1u << e;
       }
+      kn[m] = (keep | sta_nibble(m)) & valid_nibble(m);
     }
-    uint32_t vmask = 0xfu;
-    if (!FULL) {
-      vmask = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (valid(m, e)) vmask |= 1u << e;
-    }
-    kn[m] = keep | (sta_nib & vmask);
   }
   // ---- emit kept indices in ascending order: byte k of the packed scan is
   // group m0 + k (a group holds at most 128 kept blocks: no carries).  They are
