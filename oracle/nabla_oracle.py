@@ -27,6 +27,10 @@ design notes):
   R6 a query block with no kept KV block produces a zero output row.
   R7 the STA window keeps block j for row i iff |dt| <= wt, |dy| <= wh and
      |dx| <= ww on the (T, H, W) block grid, raster order, no wrap-around.
+  R13 fractal flattening is one level of P x P patches: frames in time order,
+     the patches of a frame in raster order, the tokens of a patch row-major;
+     H and W must be multiples of P (with P = 8 each 64-token block is one
+     patch of one frame).
 
 Parity pins: every function below is pinned by tests that do not reuse its
 own formula (closed forms, brute force, invariants, independent library
@@ -233,3 +237,33 @@ def block_sparse_attention(q, k, v, kv_nb, kv_inds, scale: float,
         e = np.exp(a)
         out[b, rows, hh, :] = (e @ V) / e.sum(axis=1, keepdims=True)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Fractal flattening (the step before the path).  [P1] module description and
+# NablaAttentionImpl.forward: q/k/v arrive "fractal-ordered by the model" and
+# nablaT_v2 pools 64-token blocks of that order; [P4] Methodology, "Token
+# Reordering (Fractal Flattening)": the tokens of each P x P spatial patch are
+# made contiguous while the temporal order is kept.  Reading R13.
+# ---------------------------------------------------------------------------
+def fractal_flatten(x: np.ndarray, P: int) -> np.ndarray:
+    """x [B, T, H, W, h, D] (tokens in (t, y, x) raster order) -> [B, T*H*W, h, D]
+    in fractal order."""
+    B, T, H, W = x.shape[:4]
+    if H % P or W % P:
+        raise ValueError("H and W must be multiples of P")
+    y = x.reshape(B, T, H // P, P, W // P, P, *x.shape[4:])
+    # (b, t, patch row, patch col, row in patch, col in patch, ...)
+    y = np.transpose(y, (0, 1, 2, 4, 3, 5) + tuple(range(6, y.ndim)))
+    return np.ascontiguousarray(y).reshape(B, T * H * W, *x.shape[4:])
+
+
+def fractal_unflatten(y: np.ndarray, T: int, H: int, W: int, P: int) -> np.ndarray:
+    """Inverse of fractal_flatten: [B, T*H*W, h, D] -> [B, T, H, W, h, D]."""
+    B = y.shape[0]
+    if H % P or W % P or y.shape[1] != T * H * W:
+        raise ValueError("shape mismatch")
+    x = y.reshape(B, T, H // P, W // P, P, P, *y.shape[2:])
+    x = np.transpose(x, (0, 1, 2, 4, 3, 5) + tuple(range(6, x.ndim)))
+    return np.ascontiguousarray(x).reshape(B, T, H, W, *y.shape[2:])
+

@@ -170,3 +170,41 @@ def test_attention_mutants_caught(mutant):
         except AssertionError:
             caught += 1
     assert caught > 0
+
+
+# ---- fractal flattening: plausible mistakes and the pins that catch them
+def _fractal_col_major(x, Pp):  # tokens of a patch column-major
+    B, T, H, W = x.shape[:4]
+    y = x.reshape(B, T, H // Pp, Pp, W // Pp, Pp, *x.shape[4:])
+    y = np.transpose(y, (0, 1, 2, 4, 5, 3) + tuple(range(6, y.ndim)))
+    return np.ascontiguousarray(y).reshape(B, T * H * W, *x.shape[4:])
+
+
+def _fractal_patches_col_major(x, Pp):  # patches of a frame column-major
+    B, T, H, W = x.shape[:4]
+    y = x.reshape(B, T, H // Pp, Pp, W // Pp, Pp, *x.shape[4:])
+    y = np.transpose(y, (0, 1, 4, 2, 3, 5) + tuple(range(6, y.ndim)))
+    return np.ascontiguousarray(y).reshape(B, T * H * W, *x.shape[4:])
+
+
+def _fractal_time_inside_patch(x, Pp):  # time interleaved into the patch runs
+    B, T, H, W = x.shape[:4]
+    y = x.reshape(B, T, H // Pp, Pp, W // Pp, Pp, *x.shape[4:])
+    y = np.transpose(y, (0, 2, 4, 1, 3, 5) + tuple(range(6, y.ndim)))
+    return np.ascontiguousarray(y).reshape(B, T * H * W, *x.shape[4:])
+
+
+FRACTAL_MUTANTS = [_fractal_col_major, _fractal_patches_col_major, _fractal_time_inside_patch]
+
+
+@pytest.mark.parametrize("mutant", FRACTAL_MUTANTS, ids=lambda f: f.__name__)
+def test_fractal_mutants_caught(mutant):
+    import test_oracle_fractal as TF
+
+    caught = False
+    for shape, order in TF._cases():
+        T, H, W, Pp = shape
+        x = np.arange(T * H * W).reshape(1, T, H, W, 1, 1)
+        if mutant(x, Pp).ravel().tolist() != order:
+            caught = True
+    assert caught
