@@ -297,6 +297,34 @@ def run_ours(args, w, thr):
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(w, kept_all, total_ms, args.steps)
 
+    # the steps either side of the path (SURVEY next row F2): fractal flatten of a
+    # q-sized latent and its inverse, timed on their own (not part of the step)
+    extras = None
+    if not args.no_extras:
+        T, Hs, Ws = w.grid[0], 8 * w.grid[1], 8 * w.grid[2]
+        x6 = q.view(w.B, T, Hs, Ws, w.h, w.D)
+        yf = torch.empty_like(q)
+        xr = torch.empty_like(q).view(w.B, T, Hs, Ws, w.h, w.D)
+        nbytes_q = q.numel() * q.element_size()
+        extras = {}
+        for name, fn in (("fractal_flatten", lambda: nabla.nabla_fractal_flatten(x6, 8, yf)),
+                         ("fractal_unflatten",
+                          lambda: nabla.nabla_fractal_unflatten(yf, T, Hs, Ws, 8, xr))):
+            for _ in range(3):
+                fn()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(5):
+                fn()
+            a1.record(stream)
+            torch.cuda.synchronize()
+            us = a0.elapsed_time(a1) * 1e3 / 5
+            gbs = 2 * nbytes_q / (us * 1e-6) / 1e9
+            extras[name] = {"us": us, "gbs": gbs, "bytes": 2 * nbytes_q, "bound": "hbm",
+                            "frac": gbs / load_peaks()[0]["hbm_gbs"]}
+        assert nabla.nabla_get_last_device_status() == 0
+        del yf, xr
+
     # end to end through the public API: pinned host q/k/v in, o out, every step
     e2e = None
     if not args.no_e2e:
@@ -375,6 +403,7 @@ def run_ours(args, w, thr):
                           "peak_source": f"{src} hbm"},
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "extras": extras,
         "gpu_launches": args.steps * 4,
         "clocks": clocks.summary(),
     }
@@ -393,6 +422,7 @@ def main():
     ap.add_argument("--thr", type=float, default=None)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-qblocks", type=int, default=8)
     args = ap.parse_args()
     w = W.WORKLOADS[args.workload]

@@ -128,6 +128,36 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
   return from_cuda(e);
 }
 
+static nabla_status fractal_call(const void *src, void *dst, bool flatten, nabla_dtype dt, int B,
+                                 int T, int H, int W, int h, int D, int P,
+                                 nabla_stream_t stream) {
+  using namespace nabla;
+  if (!valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
+  if (B < 1 || T < 1 || H < 1 || W < 1 || h < 1 || D < 1 || P < 1) return NABLA_ERR_INVALID_ARG;
+  if (H % P != 0 || W % P != 0) return NABLA_ERR_INVALID_ARG;
+  const double tokens = (double)B * T * H * W;
+  const size_t esz = dt == NABLA_BF16 ? 2 : 4;
+  const size_t row_bytes = (size_t)h * D * esz;
+  if (row_bytes % 16 != 0 || tokens * (double)row_bytes > 1.0e13 || tokens > 4.0e12)
+    return NABLA_ERR_INVALID_ARG;
+  if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16)) return NABLA_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)tokens * row_bytes;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(src), b0 = reinterpret_cast<uintptr_t>(dst);
+  if (a0 < b0 + bytes && b0 < a0 + bytes) return NABLA_ERR_INVALID_ARG;  // overlapping buffers
+  return from_cuda(launch_fractal(src, dst, flatten, B, T, H, W, P, row_bytes,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nabla_status nabla_fractal_flatten(const void *x, nabla_dtype dt, int B, int T, int H, int W,
+                                   int h, int D, int P, void *y, nabla_stream_t stream) {
+  return fractal_call(x, y, true, dt, B, T, H, W, h, D, P, stream);
+}
+
+nabla_status nabla_fractal_unflatten(const void *y, nabla_dtype dt, int B, int T, int H, int W,
+                                     int h, int D, int P, void *x, nabla_stream_t stream) {
+  return fractal_call(y, x, false, dt, B, T, H, W, h, D, P, stream);
+}
+
 nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
                             nabla_stream_t stream) {
   if (T < 1 || H < 1 || W < 1 || wt < 0 || wh < 0 || ww < 0 || !sta) return NABLA_ERR_INVALID_ARG;

@@ -50,6 +50,11 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
 cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
                           float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st);
 
+// Fractal token order: whole rows of row_bytes (a multiple of 16) moved between
+// [B, T, H, W, ...] raster and [B, T*H*W, ...] fractal order (flatten: raster ->
+// fractal; else the inverse).
+cudaError_t launch_fractal(const void *src, void *dst, bool flatten, int B, int T, int H, int W,
+                           int P, size_t row_bytes, cudaStream_t st);
 // K4: STA window.
 cudaError_t launch_sta(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
                        cudaStream_t st);

@@ -57,6 +57,10 @@ def load() -> ctypes.CDLL:
                                    vp, vp]
     lib.nabla_sta_mask.restype = i32
     lib.nabla_sta_mask.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp]
+    for name in ("nabla_fractal_flatten", "nabla_fractal_unflatten"):
+        fn = getattr(lib, name)
+        fn.restype = i32
+        fn.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp]
     lib.nabla_selftest_bounded_wait.restype = i32
     lib.nabla_selftest_bounded_wait.argtypes = [vp]
     lib.nabla_get_last_device_status.restype = i32
@@ -171,6 +175,34 @@ def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=Non
         out = torch.empty((s1, s1), dtype=torch.uint8, device=device or "cuda")
     _check(lib.nabla_sta_mask(T, H, W, wt, wh, ww, _ptr(out), _stream(stream)),
            "nabla_sta_mask")
+    return out
+
+
+def nabla_fractal_flatten(x: torch.Tensor, P: int = 8, out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """x [B, T, H, W, h, D] (raster token order) -> [B, T*H*W, h, D] in fractal order."""
+    if x.dim() != 6 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [B, T, H, W, h, D] tensor")
+    B, T, H, W, h, D = x.shape
+    if out is None:
+        out = torch.empty((B, T * H * W, h, D), dtype=x.dtype, device=x.device)
+    st = load().nabla_fractal_flatten(_ptr(x), _dtype_code(x), B, T, H, W, h, D, P, _ptr(out),
+                                      _stream(stream))
+    _check(st, "nabla_fractal_flatten")
+    return out
+
+
+def nabla_fractal_unflatten(y: torch.Tensor, T: int, H: int, W: int, P: int = 8,
+                            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y [B, T*H*W, h, D] in fractal order -> [B, T, H, W, h, D] in raster order."""
+    if y.dim() != 4 or y.shape[1] != T * H * W or not y.is_contiguous():
+        raise ValueError("y must be a contiguous [B, T*H*W, h, D] tensor")
+    B, _, h, D = y.shape
+    if out is None:
+        out = torch.empty((B, T, H, W, h, D), dtype=y.dtype, device=y.device)
+    st = load().nabla_fractal_unflatten(_ptr(y), _dtype_code(y), B, T, H, W, h, D, P, _ptr(out),
+                                        _stream(stream))
+    _check(st, "nabla_fractal_unflatten")
     return out
 
 

@@ -179,6 +179,32 @@ nabla_status nabla_sta_mask(int T, int H, int W, int wt, int wh, int ww, uint8_t
                             nabla_stream_t stream);
 
 /*
+ * nabla_fractal_flatten / nabla_fractal_unflatten -- the token order the path
+ * expects ([P4] Methodology, "Token Reordering (Fractal Flattening)": the tokens
+ * of each P x P spatial patch are grouped into a contiguous run, the temporal
+ * order is kept; [P1] forward: q/k/v arrive "fractal-ordered by the model" and
+ * nablaT_v2 pools 64-token blocks, so with P = 8 each block is one patch of
+ * one frame).  This library's reading of the order: frames in time order, the
+ * patches of a frame in raster order, the tokens of a patch row-major:
+ *   fractal token ((t*(H/P) + py)*(W/P) + px)*P*P + yi*P + xi
+ *   = raster token (t*H + py*P + yi)*W + px*P + xi.
+ *
+ *   x  [B, T, H, W, h, D] device, tokens in (t, y, x) raster order.
+ *   y  [B, T*H*W, h, D] device, tokens in fractal order.
+ * flatten reads x and writes y; unflatten reads y and writes x (the inverse,
+ * for the attention output).  A token's h*D elements move as one row, so any
+ * dtype works; dt fixes the element size (2 bytes bf16, 4 bytes f32).
+ * The two buffers must not overlap.  Asynchronous on `stream`.
+ * Errors: NABLA_ERR_INVALID_ARG for B, T, H, W, h, D or P < 1, H or W not a
+ * multiple of P, h*D*element size not a multiple of 16 bytes, NULL, unaligned
+ * (16 bytes) or overlapping buffers, an unknown dtype.
+ */
+nabla_status nabla_fractal_flatten(const void *x, nabla_dtype dt, int B, int T, int H, int W,
+                                   int h, int D, int P, void *y, nabla_stream_t stream);
+nabla_status nabla_fractal_unflatten(const void *y, nabla_dtype dt, int B, int T, int H, int W,
+                                     int h, int D, int P, void *x, nabla_stream_t stream);
+
+/*
  * Diagnostic of the failure-detection path (no counterpart on the pages):
  * enqueues one CTA that waits on an mbarrier nothing ever arrives on, through
  * the same bounded wait the attention kernel uses, with a 20 ms limit.  The
