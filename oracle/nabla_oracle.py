@@ -27,6 +27,9 @@ design notes):
   R6 a query block with no kept KV block produces a zero output row.
   R7 the STA window keeps block j for row i iff |dt| <= wt, |dy| <= wh and
      |dx| <= ww on the (T, H, W) block grid, raster order, no wrap-around.
+  R14 top-k selector: ties in the score at the k-th place go to the higher
+     block index (the kept set is the last k of the ascending (score, index)
+     order, as in R2); topk = min(s1, floor(topk_ratio * s1)).
   R13 fractal flattening is one level of P x P patches: frames in time order,
      the patches of a frame in raster order, the tokens of a patch row-major;
      H and W must be multiples of P (with P = 8 each 64-token block is one
@@ -266,4 +269,37 @@ def fractal_unflatten(y: np.ndarray, T: int, H: int, W: int, P: int) -> np.ndarr
     x = y.reshape(B, T, H // P, W // P, P, P, *y.shape[2:])
     x = np.transpose(x, (0, 1, 2, 4, 3, 5) + tuple(range(6, x.ndim)))
     return np.ascontiguousarray(x).reshape(B, T, H, W, *y.shape[2:])
+
+
+# ---------------------------------------------------------------------------
+# Top-k block selector (a second selector over the pooled map).  FastVideo
+# API reference, attention backends index, sla.get_block_map: the keys are
+# smoothed (k minus its mean over the sequence, per batch, head and channel),
+# q and the smoothed k are mean-pooled over 64-token blocks, the block score is
+# their plain product (no scale, no softmax), and each query block keeps the
+# topk = min(K, int(topk_ratio * K)) key blocks of largest score.  Reading R14
+# for ties; the kept blocks are listed ascending (as R3).
+# ---------------------------------------------------------------------------
+def topk_scores(q: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """q, k [B, S, h, D] -> block scores [B, h, s1, s1] (fp64)."""
+    kf = np.asarray(k, dtype=np.float64)
+    arg_k = kf - kf.mean(axis=1, keepdims=True)  # smooth-k: mean over the sequence
+    return np.matmul(pool_blocks(q), np.swapaxes(pool_blocks(arg_k), -1, -2))
+
+
+def topk_count(s1: int, topk_ratio: float) -> int:
+    return min(s1, int(topk_ratio * s1))
+
+
+def topk_mask(q: np.ndarray, k: np.ndarray, topk_ratio: float):
+    """Returns dict: kv_nb, kv_inds (ascending, -1 tail), mask, scores, topk."""
+    sc = topk_scores(q, k)
+    s1 = sc.shape[-1]
+    kk = topk_count(s1, topk_ratio)
+    order = np.argsort(sc, axis=-1, kind="stable")  # ascending (score, index)
+    keep = np.zeros(sc.shape, dtype=bool)
+    if kk > 0:
+        np.put_along_axis(keep, order[..., s1 - kk:], True, axis=-1)
+    kv_nb, kv_inds = csr_from_mask(keep)
+    return {"kv_nb": kv_nb, "kv_inds": kv_inds, "mask": keep, "scores": sc, "topk": kk}
 

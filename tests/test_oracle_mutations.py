@@ -208,3 +208,48 @@ def test_fractal_mutants_caught(mutant):
         if mutant(x, Pp).ravel().tolist() != order:
             caught = True
     assert caught
+
+
+# ---- top-k selector: plausible mistakes
+def _topk_lower_index_kept(q, k, ratio):  # ties broken toward the lower index
+    sc = O.topk_scores(q, k)
+    s1 = sc.shape[-1]
+    kk = O.topk_count(s1, ratio)
+    order = np.argsort(-sc, axis=-1, kind="stable")  # descending, lower index first
+    keep = np.zeros(sc.shape, bool)
+    if kk:
+        np.put_along_axis(keep, order[..., :kk], True, axis=-1)
+    return keep
+
+
+def _topk_rounded_count(q, k, ratio):  # round instead of int
+    sc = O.topk_scores(q, k)
+    s1 = sc.shape[-1]
+    kk = min(s1, int(round(ratio * s1)))
+    order = np.argsort(sc, axis=-1, kind="stable")
+    keep = np.zeros(sc.shape, bool)
+    if kk:
+        np.put_along_axis(keep, order[..., s1 - kk:], True, axis=-1)
+    return keep
+
+
+def _topk_smallest(q, k, ratio):  # the k smallest scores
+    sc = O.topk_scores(q, k)
+    kk = O.topk_count(sc.shape[-1], ratio)
+    order = np.argsort(sc, axis=-1, kind="stable")
+    keep = np.zeros(sc.shape, bool)
+    if kk:
+        np.put_along_axis(keep, order[..., :kk], True, axis=-1)
+    return keep
+
+
+@pytest.mark.parametrize("mutant", [_topk_lower_index_kept, _topk_rounded_count, _topk_smallest],
+                         ids=lambda f: f.__name__)
+def test_topk_mutants_caught(mutant):
+    qm = np.zeros((1, 1, 4, 2)); qm[..., 0] = 1.0
+    km = np.zeros((1, 1, 4, 2)); km[..., 0] = [3, 1, 4, 1]
+    rep = lambda m: np.repeat(np.transpose(m, (0, 2, 1, 3))[:, :, None], 64, axis=2).reshape(1, 256, 1, 2)
+    q, k = rep(qm), rep(km)
+    caught = any(not np.array_equal(mutant(q, k, r), O.topk_mask(q, k, r)["mask"])
+                 for r in (0.5, 0.7, 0.75))
+    assert caught
