@@ -308,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 2; ++h) {
             const int col0 = nt * kBN + pair * 64 + h * 32;
             if (kTma) {
+              // A piece wholly outside the map is neither staged nor stored: every
+              // staged piece commits one bulk group, so "at most one group still
+              // reading" below always means the store of the other buffer.
+              if (row0 >= P.s1 || col0 >= P.s1) continue;  // uniform over the warp
               // 128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r & 7)
               uint8_t *buf = wbuf + (pc & 1u) * kPieceBytes;
               if (lane == 0) bulk_wait_read_1();  // the store of two pieces ago has read buf
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(v[h][4 * k], v[h][4 * k + 1], v[h][4 * k + 2], v[h][4 * k + 3]);
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0 && row0 < P.s1 && col0 < P.s1) {
+              if (lane == 0) {
                 tma_store_3d(&tL, buf, col0, row0, bh);
                 bulk_commit();
               }

@@ -188,6 +188,18 @@ def test_ragged_odd_block_count(nabla):
     check_attention(nabla, w, data, nb, inds)
 
 
+@pytest.mark.parametrize("s1,grid", [(300, (3, 10, 10)), (1500, (15, 10, 10)),
+                                     (1601, (1601, 1, 1))])
+def test_partial_last_column_tile(nabla, s1, grid):
+    """s1 not a multiple of 128 (but of 4): the pooled map's last column tile has
+    32-column pieces beyond s1, which its epilogue must skip without disturbing
+    the stores still reading the staging buffers."""
+    w = W.custom(f"partial{s1}", 1, 2, 128, 64 * s1, grid, sigma=0.75, rho=0.8, thr=(0.8,))
+    data = inputs(w, seed=6)
+    nb, inds, sta = gpu_mask(nabla, w, data, 0.8)
+    check_mask(w, 0.8, data, nb, inds, sta)
+
+
 def test_head_dim_64_bf16(nabla):
     w = W.custom("d64", 1, 4, 64, 64 * 24, (2, 3, 4), sigma=0.75, thr=(0.8,))
     data = inputs(w, seed=4)
