@@ -297,8 +297,9 @@ def run_ours(args, w, thr):
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(w, kept_all, total_ms, args.steps)
 
-    # the steps either side of the path (SURVEY next row F2): fractal flatten of a
-    # q-sized latent and its inverse, timed on their own (not part of the step)
+    # beside the step, timed on their own (not part of it): the steps either side
+    # of the path, fractal flatten of a q-sized latent and its inverse, and the
+    # top-k selector
     extras = None
     if not args.no_extras:
         T, Hs, Ws = w.grid[0], 8 * w.grid[1], 8 * w.grid[2]
@@ -322,8 +323,30 @@ def run_ours(args, w, thr):
             gbs = 2 * nbytes_q / (us * 1e-6) / 1e9
             extras[name] = {"us": us, "gbs": gbs, "bytes": 2 * nbytes_q, "bound": "hbm",
                             "frac": gbs / load_peaks()[0]["hbm_gbs"]}
+        # the top-k selector on the same q, k: pool + map +
+        # top-k select; its algorithmic bytes are the mask build's without the
+        # STA window
+        ratio = 0.1
+        nb_t = torch.empty_like(kv_nb)
+        inds_t = torch.empty_like(kv_inds)
+        fn = lambda: nabla.nabla_build_mask_topk(q, k, ratio, nb_t, inds_t, ws)  # noqa: E731
+        for _ in range(3):
+            fn()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(5):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        us = a0.elapsed_time(a1) * 1e3 / 5
+        kept_t = int(nb_t.sum().item())
+        nbytes = mask_bytes(w, kept_t) - w.s1 * w.s1
+        gbs = nbytes / (us * 1e-6) / 1e9
+        extras["mask_topk"] = {"us": us, "topk_ratio": ratio, "kept_blocks": kept_t,
+                               "gbs": gbs, "bytes": nbytes, "bound": "hbm",
+                               "frac": gbs / load_peaks()[0]["hbm_gbs"]}
         assert nabla.nabla_get_last_device_status() == 0
-        del yf, xr
+        del yf, xr, nb_t, inds_t
 
     # end to end through the public API: pinned host q/k/v in, o out, every step
     e2e = None

@@ -106,6 +106,42 @@ nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int 
   return from_cuda(e);
 }
 
+nabla_status nabla_build_mask_topk(const void *q, const void *k, nabla_dtype dt, int B, int S,
+                                   int h, int D, double topk_ratio, int32_t *kv_nb,
+                                   int32_t *kv_inds, void *workspace, size_t ws_bytes,
+                                   nabla_stream_t stream) {
+  using namespace nabla;
+  if (!valid_shape(B, S, h, D) || !valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
+  if (!(topk_ratio >= 0.0) || !std::isfinite(topk_ratio)) return NABLA_ERR_INVALID_ARG;
+  if (!q || !k || !kv_nb || !kv_inds || !workspace) return NABLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(workspace, 256) || !aligned(kv_nb, 4) ||
+      !aligned(kv_inds, 4))
+    return NABLA_ERR_INVALID_ARG;
+  const Shape s{B, S, h, D, S / 64};
+  const MaskWorkspace w = mask_workspace_layout(s);
+  if (ws_bytes < w.total) return NABLA_ERR_INVALID_ARG;
+  // topk = min(s1, floor(ratio * s1)), the product formed in fp64
+  const double prod = topk_ratio * (double)s.s1;
+  const int topk = prod >= (double)s.s1 ? s.s1 : (int)std::floor(prod);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (topk == 0)
+    return from_cuda(cudaMemsetAsync(kv_nb, 0, (size_t)B * h * s.s1 * sizeof(int32_t), st));
+  char *ws = static_cast<char *>(workspace);
+  float *qa_hi = reinterpret_cast<float *>(ws + w.qa_hi);
+  float *qa_lo = reinterpret_cast<float *>(ws + w.qa_lo);
+  float *ka_hi = reinterpret_cast<float *>(ws + w.ka_hi);
+  float *ka_lo = reinterpret_cast<float *>(ws + w.ka_lo);
+  float *L = reinterpret_cast<float *>(ws + w.logits);
+  const size_t lo_off = w.mean_bytes / sizeof(float);
+  cudaError_t e;
+  int *status = device_status_ptr(&e);
+  if (!status) return NABLA_ERR_CUDA;
+  e = launch_pool(q, k, dt, s, 0, h, qa_hi, ka_hi, lo_off, st);
+  if (e == cudaSuccess) e = launch_pooled_map(qa_hi, qa_lo, ka_hi, ka_lo, s, 0, h, L, status, st);
+  if (e == cudaSuccess) e = launch_select_topk(L, s, 0, h, topk, kv_nb, kv_inds, st);
+  return from_cuda(e);
+}
+
 nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_dtype dt, int B,
                             int S, int h, int D, const int32_t *kv_nb, const int32_t *kv_inds,
                             float scale, void *o, nabla_stream_t stream) {

@@ -49,6 +49,10 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
 // K2b: row softmax, ascending running-sum cut at t = 1 - thr, STA OR, CSR emit.
 cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
                           float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st);
+// K2b, top-k selector: keep the last topk blocks of each row's ascending
+// (score, index) order of L (1 <= topk <= s1), listed ascending.
+cudaError_t launch_select_topk(const float *L, const Shape &s, int h0, int h1, int topk,
+                               int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st);
 
 // Fractal token order: whole rows of row_bytes (a multiple of 16) moved between
 // [B, T, H, W, ...] raster and [B, T*H*W, ...] fractal order (flatten: raster ->

@@ -140,7 +140,8 @@ __device__ __forceinline__ int choose_bucket(Range &r, float bmass, float tz, in
                          : (int)(((r.hi - 1u) >> sh) - d0);
   r.base += __shfl_sync(kAll, cum - bmass, bs);
   r.lo = max(r.lo, (d0 + (uint32_t)bs) << sh);
-  r.hi = min(r.hi, (d0 + (uint32_t)bs + 1u) << sh);
+  // the bucket's end can be 2^32 (top-k keys reach the top of the range)
+  r.hi = (uint32_t)min((unsigned long long)r.hi, (unsigned long long)(d0 + (uint32_t)bs + 1u) << sh);
   return bs;
 }
 
@@ -154,7 +155,7 @@ __device__ __forceinline__ int bucket_shift(const Range &r) {
 // column 128 m + 4 lane + e), then the choice of the cut bucket.  RANGED: only
 // keys in [r.lo, r.hi) count; the first pass covers every key and needs no
 // test.  Excluded elements add into the sink row, so the loop has no branches.
-template <int NV, bool FULL, bool RANGED>
+template <int NV, bool FULL, bool RANGED, bool TOPK>
 __device__ __forceinline__ void register_pass(WarpScratch &ws, const float (&p)[NV][4], Range &r,
                                               float tz, int lane, int nv, int s1) {
   const int sh = bucket_shift(r);
@@ -169,7 +170,7 @@ __device__ __forceinline__ void register_pass(WarpScratch &ws, const float (&p)[
       bool in = FULL || (m < nv && 128 * m + 4 * lane + e < s1);
       if (RANGED) in = in && u - lo < w;
       const uint32_t b = in ? (u >> sh) - d0 : (uint32_t)kBuckets;
-      ws.mass[b][lane] += p[m][e];
+      ws.mass[b][lane] += TOPK ? 1.0f : p[m][e];  // top-k: every block weighs one
     }
   __syncwarp();
   const float bmass = column_mass(ws, lane);
@@ -181,8 +182,8 @@ __device__ __forceinline__ void register_pass(WarpScratch &ws, const float (&p)[
 // how many there are.  Every element writes slot min(c, kSlots) and only an
 // in-range one advances c, so slots [0, c) hold exactly the range's blocks (a
 // later block overwrites an out-of-range write); c > kSlots means overflow,
-// detected by the caller.  The range spans < 2^26 keys (a bucket of a range
-// of keys of e in [0, 1]).
+// detected by the caller.  The range spans < 2^26 keys: a bucket of a range of
+// keys of e in [0, 1], or a top-k range narrowed to that width first.
 template <int NV, bool FULL>
 __device__ __forceinline__ int compact_range(WarpScratch &ws, const float (&p)[NV][4],
                                              const Range &r, int lane, int nv, int s1) {
@@ -209,7 +210,10 @@ __device__ __forceinline__ uint32_t entry_index(uint32_t word, int lane) {
 // so no column needs a bounds check.
 // Rows: grid.y = batch b; the launch covers rows [row0, row0 + nrows) of every
 // batch (the heads of one group), a batch being bstride = h * s1 rows apart.
-template <int NV, bool FULL>
+// TOPK: the top-k selector over raw scores (keys = order-preserving bits of the
+// score, unit mass per block, cut at count t = n - k + 1, no STA) instead of the
+// softmax / cumulative-mass cut.
+template <int NV, bool FULL, bool TOPK>
 __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     select_kernel(const float *__restrict__ L, long row0, long bstride, int nrows, int s1,
                   const uint8_t *__restrict__ sta, bool sta_words, bool vec_out, float t,
@@ -233,8 +237,9 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
 #pragma unroll
   for (int m = 0; m < NV; ++m) {
     const int j0 = 128 * m + 4 * lane;
-    sw[m] = (sta_words && (FULL || j0 < s1)) ? *reinterpret_cast<const uint32_t *>(sta_row + j0)
-                                              : 0u;
+    sw[m] = (!TOPK && sta_words && (FULL || j0 < s1))
+                ? *reinterpret_cast<const uint32_t *>(sta_row + j0)
+                : 0u;
   }
   // ---- load the row; column of element e of group m is 128 m + 4 lane + e
   float p[NV][4];
@@ -252,36 +257,60 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
       for (int e = 0; e < 4; ++e) p[m][e] = valid(m, e) ? Lr[j0 + e] : -FLT_MAX;
     }
   }
-  // ---- unnormalised softmax e = 2^(L - max) (fp32); Z = sum e
-  float mx = -FLT_MAX;
+  float tz;
+  uint32_t kmin, kmax;
+  if constexpr (TOPK) {
+    // order-preserving key of a float (sign-magnitude -> unsigned); the largest
+    // pattern is held back so that kmax + 1 does not wrap
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
 #pragma unroll
-  for (int m = 0; m < NV; ++m)
-    mx = fmaxf(mx, fmaxf(fmaxf(p[m][0], p[m][1]), fmaxf(p[m][2], p[m][3])));
-  mx = warp_max(mx);
-  float z0 = 0.f, z1 = 0.f, emin = FLT_MAX, emax = 0.f;
+    for (int m = 0; m < NV; ++m)
 #pragma unroll
-  for (int m = 0; m < NV; ++m)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (valid(m, e)) {
-        // fmaxf maps a NaN (from non-finite logits) to 0: every key then lies in
-        // [kmin, kmax], which bounds the bucket indices of the first pass
-        p[m][e] = fmaxf(exp2_approx(p[m][e] - mx), 0.f);
-        emin = fminf(emin, p[m][e]);
-        emax = fmaxf(emax, p[m][e]);
-      } else {
-        p[m][e] = 0.f;
+      for (int e = 0; e < 4; ++e) {
+        uint32_t x = __float_as_uint(p[m][e]);
+        if ((x << 1) == 0u) x = 0u;  // -0 ranks with +0 (they tie)
+        uint32_t u = min(x ^ ((x >> 31) ? 0xffffffffu : 0x80000000u), 0xfffffffeu);
+        if (!valid(m, e)) u = 0u;
+        else {
+          kmn = min(kmn, u);
+          kmx = max(kmx, u);
+        }
+        p[m][e] = __uint_as_float(u);
       }
-      if (e & 1)
-        z1 += p[m][e];
-      else
-        z0 += p[m][e];
-    }
-  const float tz = t * warp_sum(z0 + z1);
-  // e >= 0, so float order is the order of the bits
-  const uint32_t kmin = __reduce_min_sync(kAll, __float_as_uint(emin));
-  const uint32_t kmax = __reduce_max_sync(kAll, __float_as_uint(emax));
-
+    tz = t;
+    kmin = __reduce_min_sync(kAll, kmn);
+    kmax = __reduce_max_sync(kAll, kmx);
+  } else {
+    // ---- unnormalised softmax e = 2^(L - max) (fp32); Z = sum e
+    float mx = -FLT_MAX;
+  #pragma unroll
+    for (int m = 0; m < NV; ++m)
+      mx = fmaxf(mx, fmaxf(fmaxf(p[m][0], p[m][1]), fmaxf(p[m][2], p[m][3])));
+    mx = warp_max(mx);
+    float z0 = 0.f, z1 = 0.f, emin = FLT_MAX, emax = 0.f;
+  #pragma unroll
+    for (int m = 0; m < NV; ++m)
+  #pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (valid(m, e)) {
+          // fmaxf maps a NaN (from non-finite logits) to 0: every key then lies in
+          // [kmin, kmax], which bounds the bucket indices of the first pass
+          p[m][e] = fmaxf(exp2_approx(p[m][e] - mx), 0.f);
+          emin = fminf(emin, p[m][e]);
+          emax = fmaxf(emax, p[m][e]);
+        } else {
+          p[m][e] = 0.f;
+        }
+        if (e & 1)
+          z1 += p[m][e];
+        else
+          z0 += p[m][e];
+      }
+    tz = t * warp_sum(z0 + z1);
+    // e >= 0, so float order is the order of the bits
+    kmin = __reduce_min_sync(kAll, __float_as_uint(emin));
+    kmax = __reduce_max_sync(kAll, __float_as_uint(emax));
+  }
   // ---- cut: kept iff key > K, or key == K and tie rank (index order) >= R
   const bool keep_all = !(t > 0.f);
   uint32_t K = 0u;
@@ -293,7 +322,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     // a bucket of one key is a run of exact ties: running sums base + (r + 1) e_K
     // at tie ranks r = 0 .. n - 1
     auto finish_ties = [&](const Range &rr) {
-      const float ek = __uint_as_float(rr.lo);
+      const float ek = TOPK ? 1.0f : __uint_as_float(rr.lo);
       K = rr.lo;
       R = ek > 0.f ? min(max(0, (int)ceilf((tz - rr.base) / ek) - 1), rr.n - 1) : 0;
       ties_at_K = rr.n;
@@ -304,7 +333,15 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
     if (r.hi - r.lo == 1u) {
       finish_ties(r);
     } else {
-      register_pass<NV, FULL, false>(ws, p, r, tz, lane, nv, s1);
+      register_pass<NV, FULL, false, TOPK>(ws, p, r, tz, lane, nv, s1);
+      // top-k keys span up to 2^32: narrow until the range packs into a list entry
+#pragma unroll 1
+      while (TOPK && !done && r.hi - r.lo > (1u << 26)) {
+        if (r.hi - r.lo == 1u)
+          finish_ties(r);
+        else
+          register_pass<NV, FULL, true, TOPK>(ws, p, r, tz, lane, nv, s1);
+      }
       c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
       list_lo = r.lo;
       r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
@@ -318,7 +355,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
           R = 0;
           done = true;
         } else {
-          register_pass<NV, FULL, true>(ws, p, r, tz, lane, nv, s1);
+          register_pass<NV, FULL, true, TOPK>(ws, p, r, tz, lane, nv, s1);
           c = compact_range<NV, FULL>(ws, p, r, lane, nv, s1);
           list_lo = r.lo;
           r.n = (int)__reduce_add_sync(kAll, (unsigned)c);
@@ -349,7 +386,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
         if (nc <= 32) {
           // rank count: running sum at a pair = base + mass of the pairs below it
           const uint32_t my = lane < nc ? ws.cand[lane] : kAll;
-          const float ev = lane < nc ? __uint_as_float((my >> 11) + lo) : 0.f;
+          const float ev = lane < nc ? (TOPK ? 1.0f : __uint_as_float((my >> 11) + lo)) : 0.f;
           float below = 0.f;
 #pragma unroll 4
           for (int sl = 0; sl < nc; ++sl) {
@@ -388,8 +425,8 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
               }
             }
           }
-          const float pa = __uint_as_float((a >> 11) + lo);  // nc > 32: position lane is real
-          const float pb = lane + 32 < nc ? __uint_as_float((b >> 11) + lo) : 0.f;
+          const float pa = TOPK ? 1.0f : __uint_as_float((a >> 11) + lo);  // nc > 32: real
+          const float pb = lane + 32 < nc ? (TOPK ? 1.0f : __uint_as_float((b >> 11) + lo)) : 0.f;
           const float ca = warp_scan(pa, lane);
           const float cb = warp_scan(pb, lane) + __shfl_sync(kAll, ca, 31);
           const unsigned ba = __ballot_sync(kAll, r.base + ca >= tz);
@@ -421,7 +458,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
         const uint32_t key = list_lo + (ws.list[sl][lane] >> 6);
         const bool in = sl < nl && key - lo < w;
         const uint32_t b = in ? (key >> sh) - d0 : (uint32_t)kBuckets;  // else the sink
-        ws.mass[b][lane] += __uint_as_float(key);
+        ws.mass[b][lane] += TOPK ? 1.0f : __uint_as_float(key);
         ws.count[b >> 1][lane] += 1u << (16 * (b & 1u));
       }
       __syncwarp();
@@ -441,6 +478,7 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
   uint32_t kn[NV];
   const bool ranked = !keep_all && ties_at_K > 1;  // ties at the cut: rank them (rare)
   auto sta_nibble = [&](int m) -> uint32_t {
+    if (TOPK) return 0u;
     const int j0 = 128 * m + 4 * lane;
     uint32_t x = sw[m];  // STA flags of the four columns, byte e = column j0 + e
     if (!sta_words) {
@@ -542,22 +580,25 @@ struct SelectLaunch {
   int32_t *kv_nb, *kv_inds;
 };
 
-template <int NV>
+template <int NV, bool TOPK>
 void launch_nv(const SelectLaunch &a) {
   const bool words = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sta) & 3u) == 0;
   const bool vec = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.kv_inds) & 15u) == 0;
   if (a.s1 == 128 * NV)
-    select_kernel<NV, true><<<a.grid, kWarps * 32, 0, a.st>>>(
+    select_kernel<NV, true, TOPK><<<a.grid, kWarps * 32, 0, a.st>>>(
         a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
   else
-    select_kernel<NV, false><<<a.grid, kWarps * 32, 0, a.st>>>(
+    select_kernel<NV, false, TOPK><<<a.grid, kWarps * 32, 0, a.st>>>(
         a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
 }
 
 }  // namespace
 
-cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
-                          float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
+namespace {
+
+template <bool TOPK>
+cudaError_t select_dispatch(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
+                            float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
   const int nrows = (h1 - h0) * s.s1;
   SelectLaunch a{dim3((unsigned)((nrows + kWarps - 1) / kWarps), (unsigned)s.B),
                  st,
@@ -572,18 +613,33 @@ cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const 
                  kv_inds};
   const int nv = (s.s1 + 127) / 128;
   if (nv <= 1)
-    launch_nv<1>(a);
+    launch_nv<1, TOPK>(a);
   else if (nv <= 2)
-    launch_nv<2>(a);
+    launch_nv<2, TOPK>(a);
   else if (nv <= 4)
-    launch_nv<4>(a);
+    launch_nv<4, TOPK>(a);
   else if (nv <= 8)
-    launch_nv<8>(a);
+    launch_nv<8, TOPK>(a);
   else if (nv <= 12)
-    launch_nv<12>(a);
+    launch_nv<12, TOPK>(a);
   else
-    launch_nv<16>(a);
+    launch_nv<16, TOPK>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_select(const float *L, const Shape &s, int h0, int h1, const uint8_t *sta,
+                          float t, int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
+  return select_dispatch<false>(L, s, h0, h1, sta, t, kv_nb, kv_inds, st);
+}
+
+cudaError_t launch_select_topk(const float *L, const Shape &s, int h0, int h1, int topk,
+                               int32_t *kv_nb, int32_t *kv_inds, cudaStream_t st) {
+  // unit mass per block: the running count reaches s1 - topk + 1 at the first
+  // kept block; topk = s1 keeps every block (t = 0)
+  const float t = topk >= s.s1 ? 0.f : (float)(s.s1 - topk + 1);
+  return select_dispatch<true>(L, s, h0, h1, nullptr, t, kv_nb, kv_inds, st);
 }
 
 }  // namespace nabla

@@ -52,6 +52,9 @@ def load() -> ctypes.CDLL:
     lib.nabla_build_mask_noalloc.restype = i32
     lib.nabla_build_mask_noalloc.argtypes = [vp, vp, i32, i32, i32, i32, i32, vp, ctypes.c_double,
                                              vp, vp, vp]
+    lib.nabla_build_mask_topk.restype = i32
+    lib.nabla_build_mask_topk.argtypes = [vp, vp, i32, i32, i32, i32, i32, ctypes.c_double, vp,
+                                          vp, vp, sz, vp]
     lib.nabla_attn_fwd.restype = i32
     lib.nabla_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, ctypes.c_float,
                                    vp, vp]
@@ -145,6 +148,32 @@ def nabla_build_mask_noalloc(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor
     st = load().nabla_build_mask_noalloc(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
                                          float(thr), _ptr(kv_nb), _ptr(kv_inds), _stream(stream))
     _check(st, "nabla_build_mask_noalloc")
+    return kv_nb, kv_inds
+
+
+def nabla_build_mask_topk(q: torch.Tensor, k: torch.Tensor, topk_ratio: float,
+                          kv_nb: Optional[torch.Tensor] = None,
+                          kv_inds: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None, stream=None):
+    """Top-k block selector (sla.get_block_map): (q, k [B,S,h,D], topk_ratio) ->
+    (kv_nb [B,h,s1], kv_inds [B,h,s1,s1]) int32, kept blocks ascending."""
+    lib = load()
+    B, S, h, D = _shape(q)
+    if k.shape != q.shape or k.dtype != q.dtype:
+        raise ValueError("k must match q")
+    s1 = S // 64
+    dev = q.device
+    if kv_nb is None:
+        kv_nb = torch.empty((B, h, s1), dtype=torch.int32, device=dev)
+    if kv_inds is None:
+        kv_inds = torch.empty((B, h, s1, s1), dtype=torch.int32, device=dev)
+    need = lib.nabla_build_mask_workspace_bytes(B, S, h, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.nabla_build_mask_topk(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D,
+                                   float(topk_ratio), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nabla_build_mask_topk")
     return kv_nb, kv_inds
 
 

@@ -138,6 +138,39 @@ nabla_status nabla_build_mask_noalloc(const void *q, const void *k, nabla_dtype 
                                       int32_t *kv_nb, int32_t *kv_inds, nabla_stream_t stream);
 
 /*
+ * nabla_build_mask_topk -- the top-k block selector (FastVideo API reference,
+ * attention backends index, sla.get_block_map), run on the same block means
+ * and pooled map as nabla_build_mask.
+ *
+ * For every (b, h, query block i), with qa_i the mean of the 64 query tokens
+ * of block i and kc_j the mean of the 64 keys of block j after smooth-k (k
+ * minus its mean over the sequence, per batch, head and channel):
+ *   score_ij = <qa_i, kc_j>;  topk = min(s1, floor(topk_ratio * s1));
+ *   the topk blocks j of largest score_ij are kept (equal scores: the higher
+ *   block index ranks higher, i.e. the kept set is the last topk of the
+ *   ascending (score, index) order);
+ *   kv_nb / kv_inds as for nabla_build_mask (every row holds topk blocks,
+ *   listed ascending; the page's sparse_map is the row's indicator).
+ * Smooth-k subtracts <qa_i, mean k> from the whole of row i, and the pooled
+ * map's 1/sqrt(D) scale is positive, so neither changes a row's order: the
+ * library ranks the rows of the fp32 pooled map <qa_i, ka_j> / sqrt(D) that
+ * nabla_build_mask computes.  The result can differ from an exact evaluation
+ * only where two scores of a row lie within float32 rounding of each other at
+ * the topk-th place.  No STA window is applied (the page has none).
+ *
+ *   q, k        [B, S, h, D] device, element type dt.
+ *   topk_ratio  finite, >= 0; topk = 0 writes kv_nb = 0 and no kv_inds.
+ *   kv_nb, kv_inds, workspace, ws_bytes: as for nabla_build_mask (same
+ *               workspace size).
+ * Errors: NABLA_ERR_INVALID_ARG as for nabla_build_mask, and for a negative
+ * or non-finite topk_ratio.
+ */
+nabla_status nabla_build_mask_topk(const void *q, const void *k, nabla_dtype dt, int B, int S,
+                                   int h, int D, double topk_ratio, int32_t *kv_nb,
+                                   int32_t *kv_inds, void *workspace, size_t ws_bytes,
+                                   nabla_stream_t stream);
+
+/*
  * nabla_attn_fwd -- block-sparse attention forward over the kept 64x64 blocks
  * ([P1] NablaAttentionImpl.forward: flex_attention with a BlockMask of full
  * 64x64 blocks, non-causal; [P4] Expansion).

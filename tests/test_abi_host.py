@@ -33,7 +33,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for n in ["nabla_build_mask", "nabla_attn_fwd", "nabla_sta_mask",
+    for n in ["nabla_build_mask", "nabla_build_mask_topk", "nabla_attn_fwd", "nabla_sta_mask",
               "nabla_build_mask_workspace_bytes", "nabla_get_last_device_status",
               "nabla_status_string", "nabla_abi_version"]:
         assert n in names
@@ -94,6 +94,25 @@ def _mask(lib, **kw):
                          ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
 def test_build_mask_rejects(lib, kw):
     assert _mask(lib, **kw) == INVALID
+
+
+def _topk(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, dt=1, B=1, S=1024, h=2, D=64, ratio=0.25, nb=FAKE, inds=FAKE,
+             ws=FAKE, wsb=1 << 30, st=None)
+    a.update(kw)
+    return lib.nabla_build_mask_topk(a["q"], a["k"], a["dt"], a["B"], a["S"], a["h"], a["D"],
+                                     a["ratio"], a["nb"], a["inds"], a["ws"], a["wsb"], a["st"])
+
+
+@pytest.mark.parametrize("kw", [dict(S=1000), dict(D=96), dict(B=0), dict(h=0),
+                                dict(ratio=-0.1), dict(ratio=float("nan")),
+                                dict(ratio=float("inf")), dict(q=None), dict(k=None),
+                                dict(nb=None), dict(inds=None), dict(ws=None), dict(k=FAKE + 8),
+                                dict(ws=FAKE + 16), dict(inds=FAKE + 2), dict(wsb=100),
+                                dict(dt=7)],
+                         ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_build_mask_topk_rejects(lib, kw):
+    assert _topk(lib, **kw) == INVALID
 
 
 def _attn(lib, **kw):
