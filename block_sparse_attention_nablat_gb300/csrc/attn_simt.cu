@@ -15,6 +15,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nabla {
 namespace {
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T *__restrict__ q,
   const int tid = threadIdx.x, r = tid >> 2, part = tid & 3;
   const size_t row_stride = (size_t)h * D;
   const size_t head_off = (size_t)b * S * row_stride + (size_t)hh * D;
+  pdl_launch_dependents();
+  pdl_wait();  // kv_nb / kv_inds and q, k, v are written; no earlier kernel still reads o
 
   for (int e = tid; e < 64 * D; e += 256) {
     const int rr = e / D, d = e - rr * D;
@@ -131,10 +134,9 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const Shap
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(s.s1, s.h, s.B);
-  kern<<<grid, 256, smem, st>>>(static_cast<const T *>(q), static_cast<const T *>(k),
-                                static_cast<const T *>(v), s.S, s.h, kv_nb, kv_inds,
-                                scale * 1.4426950408889634f, static_cast<T *>(o), status);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(256), smem, st, static_cast<const T *>(q),
+                    static_cast<const T *>(k), static_cast<const T *>(v), s.S, s.h, kv_nb, kv_inds,
+                    scale * 1.4426950408889634f, static_cast<T *>(o), status);
 }
 
 }  // namespace

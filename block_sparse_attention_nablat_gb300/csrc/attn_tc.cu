@@ -52,6 +52,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "pdl.cuh"
 #include "tc_ptx.cuh"
 
 namespace nabla {
@@ -799,6 +800,7 @@ __global__ void __launch_bounds__(384, 1)
   uint32_t *tmem_slot = &sync->tmem_slot;
   volatile int *abort = &sync->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kKStages; ++i) {
@@ -833,6 +835,7 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // kv_nb / kv_inds and q, k, v are written; no earlier kernel still reads o
   // the K / V staging area is free until the producer starts
   static_assert(sizeof(StrideScratch) <= (size_t)C::kOffInfo - C::kOffK, "stride scratch fits");
   Params Pp = P;
@@ -901,8 +904,7 @@ cudaError_t launch_d(const void *q, const void *k, const void *v, const Shape &s
   const int grid = (int)(units < sms ? units : sms);
   Params p{static_cast<__nv_bfloat16 *>(o), kv_nb, kv_inds, s.B, s.S, s.h,
            scale * 1.4426950408889634f, status, 1};
-  kern<<<grid, C::kThreads, smem_bytes<D>(), st>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem_bytes<D>(), st, mq, mk, mv, p);
 }
 
 }  // namespace

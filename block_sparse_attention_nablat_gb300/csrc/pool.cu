@@ -20,6 +20,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nabla {
 namespace {
@@ -87,6 +88,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const T *__restrict__ q,
                                                    float *__restrict__ ka, size_t lo_off) {
   constexpr int E = Chunk<T>::kElems;
   __shared__ float part[kRowGroups][kChunksPerCta * E];
+  pdl_launch_dependents();
+  pdl_wait();  // q and k are written, and no earlier kernel still reads qa / ka
 
   const int i = blockIdx.x;
   const int b = blockIdx.z >> 1;
@@ -142,14 +145,12 @@ cudaError_t launch_pool(const void *q, const void *k, nabla_dtype dt, const Shap
   const float q_scale = (float)(1.4426950408889634 / sqrt((double)s.D));
   dim3 grid(s.s1, (c1 - c0 + kChunksPerCta - 1) / kChunksPerCta, 2 * s.B);
   if (dt == NABLA_BF16)
-    pool_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k), s.S, s.h,
-        s.D, c0, c1, q_scale, qa, ka, lo_off);
-  else
-    pool_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float *>(q),
-                                             static_cast<const float *>(k), s.S, s.h, s.D, c0,
-                                             c1, q_scale, qa, ka, lo_off);
-  return cudaGetLastError();
+    return launch_pdl(pool_kernel<__nv_bfloat16>, grid, dim3(256), 0, st,
+                      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                      s.S, s.h, s.D, c0, c1, q_scale, qa, ka, lo_off);
+  return launch_pdl(pool_kernel<float>, grid, dim3(256), 0, st, static_cast<const float *>(q),
+                    static_cast<const float *>(k), s.S, s.h, s.D, c0, c1, q_scale, qa, ka,
+                    lo_off);
 }
 
 }  // namespace nabla

@@ -36,6 +36,7 @@
 #include <cudaTypedefs.h>
 
 #include "internal.h"
+#include "pdl.cuh"
 #include "tc_ptx.cuh"
 
 namespace nabla {
@@ -136,6 +137,7 @@ template <bool kTma>
 __global__ void __launch_bounds__(kThreads, 1)
     pooled_map_kernel(const __grid_constant__ CUtensorMap tKh, const __grid_constant__ CUtensorMap tKl,
                       const __grid_constant__ CUtensorMap tL, MapParams P) {
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sync->tmem_slot;
+  pdl_wait();  // the block means are written; no earlier kernel still reads L
 
   if (warp == 0 && lane == 0) {
     // ---- TMA producer: B chunks of every tile of every strip
@@ -417,8 +420,7 @@ cudaError_t launch_pooled_map(const float *qa_hi, const float *qa_lo, const floa
               status};
   const long strips = (long)p.units * p.mt;
   const int grid = (int)(strips < sms ? strips : sms);
-  kernel<<<grid, kThreads, kSmemBytes, st>>>(tKh, tKl, tL, p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(kThreads), kSmemBytes, st, tKh, tKl, tL, p);
 }
 
 }  // namespace nabla

@@ -34,6 +34,7 @@
 #include <cfloat>
 
 #include "internal.h"
+#include "pdl.cuh"
 
 namespace nabla {
 namespace {
@@ -219,9 +220,11 @@ __global__ void __launch_bounds__(kWarps * 32, NV > 12 ? 4 : 5)
                   const uint8_t *__restrict__ sta, bool sta_words, bool vec_out, float t,
                   int32_t *__restrict__ kv_nb, int32_t *__restrict__ kv_inds) {
   __shared__ __align__(16) WarpScratch scratch[kWarps];  // 16-byte reads and writes
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int local = blockIdx.x * kWarps + warp;
   if (local >= nrows) return;  // uniform per warp
+  pdl_wait();  // L is written; no earlier kernel still reads kv_nb / kv_inds
   const long row = blockIdx.y * bstride + row0 + local;
   WarpScratch &ws = scratch[warp];
   const int i = (int)(row % s1);
@@ -581,15 +584,12 @@ struct SelectLaunch {
 };
 
 template <int NV, bool TOPK>
-void launch_nv(const SelectLaunch &a) {
+cudaError_t launch_nv(const SelectLaunch &a) {
   const bool words = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.sta) & 3u) == 0;
   const bool vec = (a.s1 & 3) == 0 && (reinterpret_cast<uintptr_t>(a.kv_inds) & 15u) == 0;
-  if (a.s1 == 128 * NV)
-    select_kernel<NV, true, TOPK><<<a.grid, kWarps * 32, 0, a.st>>>(
-        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
-  else
-    select_kernel<NV, false, TOPK><<<a.grid, kWarps * 32, 0, a.st>>>(
-        a.L, a.row0, a.bstride, a.nrows, a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
+  auto kern = a.s1 == 128 * NV ? select_kernel<NV, true, TOPK> : select_kernel<NV, false, TOPK>;
+  return launch_pdl(kern, a.grid, dim3(kWarps * 32), 0, a.st, a.L, a.row0, a.bstride, a.nrows,
+                    a.s1, a.sta, words, vec, a.t, a.kv_nb, a.kv_inds);
 }
 
 }  // namespace
@@ -612,19 +612,12 @@ cudaError_t select_dispatch(const float *L, const Shape &s, int h0, int h1, cons
                  kv_nb,
                  kv_inds};
   const int nv = (s.s1 + 127) / 128;
-  if (nv <= 1)
-    launch_nv<1, TOPK>(a);
-  else if (nv <= 2)
-    launch_nv<2, TOPK>(a);
-  else if (nv <= 4)
-    launch_nv<4, TOPK>(a);
-  else if (nv <= 8)
-    launch_nv<8, TOPK>(a);
-  else if (nv <= 12)
-    launch_nv<12, TOPK>(a);
-  else
-    launch_nv<16, TOPK>(a);
-  return cudaGetLastError();
+  if (nv <= 1) return launch_nv<1, TOPK>(a);
+  if (nv <= 2) return launch_nv<2, TOPK>(a);
+  if (nv <= 4) return launch_nv<4, TOPK>(a);
+  if (nv <= 8) return launch_nv<8, TOPK>(a);
+  if (nv <= 12) return launch_nv<12, TOPK>(a);
+  return launch_nv<16, TOPK>(a);
 }
 
 }  // namespace

@@ -23,6 +23,12 @@
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) of the CURRENT device.  A returned NABLA_OK means
  *     the arguments were valid and the kernels were launched.
+ *   - The mask and attention kernels are launched with programmatic dependent
+ *     launch: each lets the next kernel of the stream start its prologue early
+ *     and waits for the previous kernel to complete before it touches device
+ *     memory, so stream order is kept whatever precedes the call.  Setting
+ *     NABLA_DISABLE_PDL=1 in the environment (read once per process) gives
+ *     plain launches.
  *   - Errors are returned, never raised on the device: invalid arguments are
  *     rejected on the host before anything is launched; launch failures give
  *     NABLA_ERR_CUDA; device-side conditions (a bounded wait that gave up, an
