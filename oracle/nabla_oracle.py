@@ -34,6 +34,8 @@ design notes):
      the patches of a frame in raster order, the tokens of a patch row-major;
      H and W must be multiples of P (with P = 8 each 64-token block is one
      patch of one frame).
+  R17 backward: delta_s = dout_s . o_s is formed from the o passed in (the
+     stored forward output) when one is given, else from the exact o.
 
 Parity pins: every function below is pinned by tests that do not reuse its
 own formula (closed forms, brute force, invariants, independent library
@@ -240,6 +242,56 @@ def block_sparse_attention(q, k, v, kv_nb, kv_inds, scale: float,
         e = np.exp(a)
         out[b, rows, hh, :] = (e @ V) / e.sum(axis=1, keepdims=True)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Backward of a7 (training).  gist.science NABLA summary, "Dual-Phase
+# Acceleration" and Experimental Results (pre-training iteration time): the
+# method is used for training, where flex_attention ([P1] forward) is
+# differentiated by autograd.  The plain definition is the gradient of the
+# masked softmax attention of a7 with respect to q, k and v, for an upstream
+# gradient dout of o.  With z = scale * q k^T over the kept tokens J of a row,
+# P = softmax(z), o = P v:
+#   dv_u = sum_s P_su dout_s            dP_su = dout_s . v_u
+#   delta_s = sum_u P_su dP_su = dout_s . o_s
+#   dz_su = P_su (dP_su - delta_s)
+#   dq_s = scale sum_u dz_su k_u        dk_u = scale sum_s dz_su q_s
+# Rows with nothing kept (R6) contribute nothing.  Reading R17: when o is
+# passed, delta_s is formed from that o (dout_s . o_s), as a training step
+# does with the forward output it stored; otherwise from the exact o.
+# ---------------------------------------------------------------------------
+def block_sparse_attention_bwd(q, k, v, dout, kv_nb, kv_inds, scale: float, o=None):
+    """(dq, dk, dv), float64 [B, S, h, D] each."""
+    B, S, h, D = q.shape
+    s1 = S // BLOCK
+    dq = np.zeros((B, S, h, D), dtype=np.float64)
+    dk = np.zeros((B, S, h, D), dtype=np.float64)
+    dv = np.zeros((B, S, h, D), dtype=np.float64)
+    for b in range(B):
+        for hh in range(h):
+            for i in range(s1):
+                n = int(kv_nb[b, hh, i])
+                if n == 0:
+                    continue
+                rows = slice(i * BLOCK, (i + 1) * BLOCK)
+                blocks = np.asarray(kv_inds[b, hh, i, :n], dtype=np.int64)
+                tok = (blocks[:, None] * BLOCK + np.arange(BLOCK)[None, :]).ravel()
+                Q = q[b, rows, hh, :].astype(np.float64)
+                K = k[b, tok, hh, :].astype(np.float64)
+                V = v[b, tok, hh, :].astype(np.float64)
+                dO = dout[b, rows, hh, :].astype(np.float64)
+                z = scale * (Q @ K.T)
+                z -= z.max(axis=1, keepdims=True)
+                P = np.exp(z)
+                P /= P.sum(axis=1, keepdims=True)
+                O = P @ V if o is None else o[b, rows, hh, :].astype(np.float64)
+                dP = dO @ V.T
+                delta = (dO * O).sum(axis=1, keepdims=True)
+                dz = P * (dP - delta)
+                dq[b, rows, hh, :] = scale * (dz @ K)
+                dk[b, tok, hh, :] += scale * (dz.T @ Q)
+                dv[b, tok, hh, :] += P.T @ dO
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------------------

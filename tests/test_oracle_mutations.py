@@ -253,3 +253,57 @@ def test_topk_mutants_caught(mutant):
     caught = any(not np.array_equal(mutant(q, k, r), O.topk_mask(q, k, r)["mask"])
                  for r in (0.5, 0.7, 0.75))
     assert caught
+
+
+# ---- attention backward: plausible mistakes, each caught by the finite-difference pin
+def _bwd_variant(kind, q, k, v, dout, nb, inds, scale):
+    B, S, h, D = q.shape
+    dq, dk, dv = (np.zeros((B, S, h, D)) for _ in range(3))
+    for b in range(B):
+        for hh in range(h):
+            for i in range(S // 64):
+                n = int(nb[b, hh, i])
+                if n == 0:
+                    continue
+                rows = slice(64 * i, 64 * i + 64)
+                tok = (inds[b, hh, i, :n][:, None] * 64 + np.arange(64)[None, :]).ravel()
+                Q, K, V, dO = q[b, rows, hh], k[b, tok, hh], v[b, tok, hh], dout[b, rows, hh]
+                z = scale * Q @ K.T
+                P = np.exp(z - z.max(1, keepdims=True))
+                P /= P.sum(1, keepdims=True)
+                dP = dO @ V.T
+                delta = (dP.sum(1, keepdims=True) if kind == "delta_from_dp"
+                         else (dO * (P @ V)).sum(1, keepdims=True))
+                dz = P * (delta - dP) if kind == "sign" else P * (dP - delta)
+                dq[b, rows, hh] = scale * dz @ (V if kind == "dq_uses_v" else K)
+                dk[b, tok, hh] += (1.0 if kind == "no_scale_dk" else scale) * dz.T @ Q
+                dv[b, tok, hh] += P.T @ dO
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("kind", ["no_scale_dk", "delta_from_dp", "sign", "dq_uses_v"])
+def test_backward_mutants_caught(kind):
+    rng = np.random.default_rng(5)
+    B, h, D, S = 1, 1, 4, 128
+    q, k, v, dout = (rng.standard_normal((B, S, h, D)) for _ in range(4))
+    nb = np.array([[[2, 1]]], np.int32)
+    inds = np.array([[[[0, 1], [1, -1]]]], np.int32)
+    scale = 0.6
+    got = _bwd_variant(kind, q, k, v, dout, nb, inds, scale)
+    eps = 1e-6
+
+    def loss(qq, kk, vv):
+        return float((dout * O.block_sparse_attention(qq, kk, vv, nb, inds, scale)).sum())
+
+    caught = False
+    for t, g in enumerate(got):
+        for _ in range(12):
+            ix = tuple(int(rng.integers(n)) for n in q.shape)
+            args = [q.copy(), k.copy(), v.copy()]
+            args[t][ix] += eps
+            fp = loss(*args)
+            args[t][ix] -= 2 * eps
+            fm = loss(*args)
+            if abs((fp - fm) / (2 * eps) - g[ix]) > 1e-5:
+                caught = True
+    assert caught
