@@ -164,6 +164,38 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
   return from_cuda(e);
 }
 
+size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D) {
+  if (!nabla::valid_shape(B, S, h, D)) return 0;
+  return nabla::bwd_workspace_layout(Shape{B, S, h, D, S / 64}).total;
+}
+
+nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, nabla_dtype dt, int B, int S, int h, int D,
+                            const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
+                            void *dk, void *dv, void *workspace, size_t ws_bytes,
+                            nabla_stream_t stream) {
+  using namespace nabla;
+  if (!valid_shape(B, S, h, D) || !valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return NABLA_ERR_INVALID_ARG;
+  const void *in[] = {q, k, v, o, dout};
+  void *out[] = {dq, dk, dv};
+  for (const void *p : in)
+    if (!p || !aligned(p, 16)) return NABLA_ERR_INVALID_ARG;
+  for (void *p : out)
+    if (!p || !aligned(p, 16)) return NABLA_ERR_INVALID_ARG;
+  if (!kv_nb || !kv_inds || !workspace || !aligned(kv_nb, 4) || !aligned(kv_inds, 4) ||
+      !aligned(workspace, 256))
+    return NABLA_ERR_INVALID_ARG;
+  const Shape s{B, S, h, D, S / 64};
+  if (ws_bytes < bwd_workspace_layout(s).total) return NABLA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  int *status = device_status_ptr(&e);
+  if (!status) return NABLA_ERR_CUDA;
+  return from_cuda(launch_attn_bwd(q, k, v, o, dout, dt, s, kv_nb, kv_inds, scale, dq, dk, dv,
+                                   workspace, status, st));
+}
+
 static nabla_status fractal_call(const void *src, void *dst, bool flatten, nabla_dtype dt, int B,
                                  int T, int H, int W, int h, int D, int P,
                                  nabla_stream_t stream) {

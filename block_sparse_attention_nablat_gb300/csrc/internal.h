@@ -62,6 +62,18 @@ cudaError_t launch_fractal(const void *src, void *dst, bool flatten, int B, int 
 // K4: STA window.
 cudaError_t launch_sta(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta,
                        cudaStream_t st);
+// K7: block-sparse attention backward.  Workspace regions (bytes, 256-aligned):
+// lse2 and delta [B, h, S] fp32, the transposed CSR qt_nb [B, h, s1] and
+// qt_inds [B, h, s1, s1] int32, and the word rows [B, h, s1, words] uint32.
+struct BwdWorkspace {
+  size_t lse2, delta, qt_nb, qt_inds, bits, total;
+  int words;
+};
+BwdWorkspace bwd_workspace_layout(const Shape &s);
+cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, nabla_dtype dt, const Shape &s,
+                            const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
+                            void *dk, void *dv, void *workspace, int *status, cudaStream_t st);
 // K3f: CUDA-core block-sparse attention (fp32 storage).
 cudaError_t launch_attn_simt(const void *q, const void *k, const void *v, nabla_dtype dt,
                              const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,

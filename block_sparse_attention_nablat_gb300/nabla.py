@@ -58,6 +58,11 @@ def load() -> ctypes.CDLL:
     lib.nabla_attn_fwd.restype = i32
     lib.nabla_attn_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, ctypes.c_float,
                                    vp, vp]
+    lib.nabla_attn_bwd_workspace_bytes.restype = sz
+    lib.nabla_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.nabla_attn_bwd.restype = i32
+    lib.nabla_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                   ctypes.c_float, vp, vp, vp, vp, sz, vp]
     lib.nabla_sta_mask.restype = i32
     lib.nabla_sta_mask.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp]
     for name in ("nabla_fractal_flatten", "nabla_fractal_unflatten"):
@@ -193,6 +198,37 @@ def nabla_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb: tor
                             _ptr(kv_inds), float(scale), _ptr(o), _stream(stream))
     _check(st, "nabla_attn_fwd")
     return o
+
+
+def nabla_attn_bwd_workspace_bytes(B: int, S: int, h: int, D: int) -> int:
+    return load().nabla_attn_bwd_workspace_bytes(B, S, h, D)
+
+
+def nabla_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
+                   dout: torch.Tensor, kv_nb: torch.Tensor, kv_inds: torch.Tensor,
+                   scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
+                   dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Gradients of nabla_attn_fwd: returns (dq, dk, dv), each [B,S,h,D] in q's dtype."""
+    lib = load()
+    B, S, h, D = _shape(q)
+    for t in (k, v, o, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("k, v, o, dout must match q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = lib.nabla_attn_bwd_workspace_bytes(B, S, h, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.nabla_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _dtype_code(q), B, S,
+                            h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(dq), _ptr(dk),
+                            _ptr(dv), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "nabla_attn_bwd")
+    return dq, dk, dv
 
 
 def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=None,

@@ -167,6 +167,13 @@ def generate(w: Workload, seed: int = 0) -> Dict[str, np.ndarray]:
     return out
 
 
+def generate_dout(w: Workload, seed: int = 0) -> np.ndarray:
+    """An upstream gradient for the backward: N(0,1) tokens [B, S, h, D] drawn
+    from its own stream (SeedSequence((seed, 1))), in the workload's storage type."""
+    x = _noise(np.random.SeedSequence((seed, 1)), w, None)
+    return f32_to_bf16_bits(x) if w.dtype == "bf16" else x
+
+
 def as_float(x: np.ndarray) -> np.ndarray:
     """Storage array (float32 or bf16 bits) -> exact float32 values."""
     if x.dtype == np.uint16:

@@ -205,6 +205,43 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
                             float scale, void *o, nabla_stream_t stream);
 
 /*
+ * nabla_attn_bwd -- gradients of nabla_attn_fwd with respect to q, k and v
+ * (gist.science NABLA summary, "Dual-Phase Acceleration" and Experimental
+ * Results: the method trains with the block mask, so the forward is
+ * differentiated; [P1] NablaAttentionImpl.forward is the function).
+ *
+ * For every (b, hh) and query token s in block i, J the tokens of the kept
+ * blocks of row i, z_su = scale <q_s, k_u>, P = softmax_u(z), and the upstream
+ * gradient dout:
+ *   dv_u = sum_s P_su dout_s              dP_su = <dout_s, v_u>
+ *   delta_s = <dout_s, o_s>               dz_su = P_su (dP_su - delta_s)
+ *   dq_s = scale sum_u dz_su k_u          dk_u = scale sum_s dz_su q_s
+ * where the sums over s run over every query row whose block kept u's block.
+ * Rows with kv_nb = 0 contribute nothing (their dq is 0); key blocks that no
+ * row kept get dk = dv = 0.  delta is formed from the o passed in, which
+ * must be the forward output for the same inputs (as stored by a training
+ * step).  Arithmetic is fp32 on CUDA cores; dq, dk, dv are written in dt.
+ *
+ *   q, k, v, o, dout  [B, S, h, D] device, element type dt.
+ *   kv_nb, kv_inds    the mask, as for nabla_attn_fwd (bad entries are skipped
+ *                     and reported as NABLA_ERR_BAD_INDEX).
+ *   scale             the forward's softmax scale.
+ *   dq, dk, dv        [B, S, h, D] device, element type dt, overwritten.
+ *   workspace         device scratch of ws_bytes >= nabla_attn_bwd_workspace_bytes()
+ *                     (256-byte aligned): the rows' log-sum-exp and delta, and
+ *                     the transposed mask (for each key block, the query
+ *                     blocks that kept it).
+ * Errors: NABLA_ERR_INVALID_ARG as for nabla_attn_fwd, for NULL or unaligned
+ * o, dout, dq, dk, dv or workspace, and for a short workspace.
+ */
+size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D);
+nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, nabla_dtype dt, int B, int S, int h, int D,
+                            const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
+                            void *dk, void *dv, void *workspace, size_t ws_bytes,
+                            nabla_stream_t stream);
+
+/*
  * nabla_sta_mask -- the spatio-temporal window ([P1] NablaAttentionMetadata
  * "sta_mask"; [P4] Hybrid Integration with STA).  The pages do not show its
  * construction; this library's reading: on the (T, H, W) block grid with

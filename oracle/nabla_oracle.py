@@ -260,37 +260,42 @@ def block_sparse_attention(q, k, v, kv_nb, kv_inds, scale: float,
 # passed, delta_s is formed from that o (dout_s . o_s), as a training step
 # does with the forward output it stored; otherwise from the exact o.
 # ---------------------------------------------------------------------------
-def block_sparse_attention_bwd(q, k, v, dout, kv_nb, kv_inds, scale: float, o=None):
-    """(dq, dk, dv), float64 [B, S, h, D] each."""
+def block_sparse_attention_bwd(q, k, v, dout, kv_nb, kv_inds, scale: float, o=None,
+                               qblocks: Optional[Iterable[Tuple[int, int, int]]] = None):
+    """(dq, dk, dv), float64 [B, S, h, D] each.
+
+    qblocks restricts the sums over query rows to the listed (b, h, i) blocks:
+    dq is then exact for those blocks (0 elsewhere), and dk, dv of a key block
+    are exact when every block that kept it is listed."""
     B, S, h, D = q.shape
     s1 = S // BLOCK
     dq = np.zeros((B, S, h, D), dtype=np.float64)
     dk = np.zeros((B, S, h, D), dtype=np.float64)
     dv = np.zeros((B, S, h, D), dtype=np.float64)
-    for b in range(B):
-        for hh in range(h):
-            for i in range(s1):
-                n = int(kv_nb[b, hh, i])
-                if n == 0:
-                    continue
-                rows = slice(i * BLOCK, (i + 1) * BLOCK)
-                blocks = np.asarray(kv_inds[b, hh, i, :n], dtype=np.int64)
-                tok = (blocks[:, None] * BLOCK + np.arange(BLOCK)[None, :]).ravel()
-                Q = q[b, rows, hh, :].astype(np.float64)
-                K = k[b, tok, hh, :].astype(np.float64)
-                V = v[b, tok, hh, :].astype(np.float64)
-                dO = dout[b, rows, hh, :].astype(np.float64)
-                z = scale * (Q @ K.T)
-                z -= z.max(axis=1, keepdims=True)
-                P = np.exp(z)
-                P /= P.sum(axis=1, keepdims=True)
-                O = P @ V if o is None else o[b, rows, hh, :].astype(np.float64)
-                dP = dO @ V.T
-                delta = (dO * O).sum(axis=1, keepdims=True)
-                dz = P * (dP - delta)
-                dq[b, rows, hh, :] = scale * (dz @ K)
-                dk[b, tok, hh, :] += scale * (dz.T @ Q)
-                dv[b, tok, hh, :] += P.T @ dO
+    if qblocks is None:
+        qblocks = [(b, hh, i) for b in range(B) for hh in range(h) for i in range(s1)]
+    for b, hh, i in qblocks:
+        n = int(kv_nb[b, hh, i])
+        if n == 0:
+            continue
+        rows = slice(i * BLOCK, (i + 1) * BLOCK)
+        blocks = np.asarray(kv_inds[b, hh, i, :n], dtype=np.int64)
+        tok = (blocks[:, None] * BLOCK + np.arange(BLOCK)[None, :]).ravel()
+        Q = q[b, rows, hh, :].astype(np.float64)
+        K = k[b, tok, hh, :].astype(np.float64)
+        V = v[b, tok, hh, :].astype(np.float64)
+        dO = dout[b, rows, hh, :].astype(np.float64)
+        z = scale * (Q @ K.T)
+        z -= z.max(axis=1, keepdims=True)
+        P = np.exp(z)
+        P /= P.sum(axis=1, keepdims=True)
+        O = P @ V if o is None else o[b, rows, hh, :].astype(np.float64)
+        dP = dO @ V.T
+        delta = (dO * O).sum(axis=1, keepdims=True)
+        dz = P * (dP - delta)
+        dq[b, rows, hh, :] = scale * (dz @ K)
+        dk[b, tok, hh, :] += scale * (dz.T @ Q)
+        dv[b, tok, hh, :] += P.T @ dO
     return dq, dk, dv
 
 

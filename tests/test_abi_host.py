@@ -131,6 +131,38 @@ def test_attn_rejects(lib, kw):
     assert _attn(lib, **kw) == INVALID
 
 
+def _bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, g=FAKE, dt=1, B=1, S=1024, h=2, D=64, nb=FAKE,
+             inds=FAKE, scale=0.125, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, wsb=1 << 30, st=None)
+    a.update(kw)
+    return lib.nabla_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["g"], a["dt"], a["B"], a["S"],
+                              a["h"], a["D"], a["nb"], a["inds"], a["scale"], a["dq"], a["dk"],
+                              a["dv"], a["ws"], a["wsb"], a["st"])
+
+
+@pytest.mark.parametrize("kw", [dict(S=1000), dict(D=32), dict(B=0), dict(o=None), dict(g=None),
+                                dict(dq=None), dict(dk=FAKE + 4), dict(dv=None), dict(ws=None),
+                                dict(ws=FAKE + 64), dict(wsb=1000), dict(nb=FAKE + 2),
+                                dict(scale=float("nan")), dict(dt=3)],
+                         ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_attn_bwd_rejects(lib, kw):
+    assert _bwd(lib, **kw) == INVALID
+
+
+@pytest.mark.parametrize("shape", [(1, 1024, 2, 64), (1, 98304, 24, 128), (2, 64 * 37, 3, 128)])
+def test_attn_bwd_workspace_bytes(lib, shape):
+    B, S, h, D = shape
+    s1 = S // 64
+
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    want = 2 * up(B * h * S * 4) + up(B * h * s1 * 4) + up(B * h * s1 * s1 * 4) + \
+        up(B * h * s1 * ((s1 + 31) // 32) * 4)
+    assert lib.nabla_attn_bwd_workspace_bytes(*shape) == want
+    assert lib.nabla_attn_bwd_workspace_bytes(1, 1000, 2, 64) == 0
+
+
 @pytest.mark.parametrize("args", [(0, 2, 2, 1, 1, 1), (4, 2, 2, -1, 1, 1), (64, 8, 8, 1, 1, 1)])
 def test_sta_rejects(lib, args):
     assert lib.nabla_sta_mask(*args, FAKE, None) == INVALID
