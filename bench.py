@@ -347,6 +347,28 @@ def run_ours(args, w, thr):
                                "frac": gbs / load_peaks()[0]["hbm_gbs"]}
         assert nabla.nabla_get_last_device_status() == 0
         del yf, xr, nb_t, inds_t
+        # the attention backward (CUDA cores) on the same inputs and mask, with a
+        # seeded upstream gradient; algorithmic FLOPs: the five 64x64xD products
+        # of a kept block (S, dP, dV, dK, dQ), though the kernels run eight
+        g = nabla.from_storage(W.generate_dout(w, seed=rank), dev)
+        bws = torch.empty(nabla.nabla_attn_bwd_workspace_bytes(w.B, w.S, w.h, w.D),
+                          dtype=torch.uint8, device=dev)
+        grads = [torch.empty_like(q) for _ in range(3)]
+        nabla.nabla_attn_bwd(q, k, v, o, g, kv_nb, kv_inds, w.scale, *grads, bws)  # warm-up
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        nabla.nabla_attn_bwd(q, k, v, o, g, kv_nb, kv_inds, w.scale, *grads, bws)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        bms = a0.elapsed_time(a1)
+        bflops = 5.0 * 2 * 64 * 64 * w.D * kept
+        extras["attn_bwd"] = {"ms": bms, "tflops_kept": bflops / bms / 1e9, "bound": "tensor",
+                              "frac": bflops / bms / 1e9 / load_peaks()[0][
+                                  "bf16_tflops_sustained"],
+                              "note": "CUDA-core fp32 kernels; the frac is of the bf16 "
+                                      "tensor peak"}
+        assert nabla.nabla_get_last_device_status() == 0
+        del g, bws, grads
 
     # end to end through the public API: pinned host q/k/v in, o out, every step
     e2e = None
