@@ -9,7 +9,7 @@ namespace nabla {
 
 cudaError_t launch_attn_tc(const void *q, const void *k, const void *v, const Shape &s,
                            const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *o,
-                           int *status, cudaStream_t st);
+                           float *lse, int *status, cudaStream_t st);
 
 namespace {
 
@@ -142,15 +142,16 @@ nabla_status nabla_build_mask_topk(const void *q, const void *k, nabla_dtype dt,
   return from_cuda(e);
 }
 
-nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_dtype dt, int B,
-                            int S, int h, int D, const int32_t *kv_nb, const int32_t *kv_inds,
-                            float scale, void *o, nabla_stream_t stream) {
+static nabla_status attn_fwd_call(const void *q, const void *k, const void *v, nabla_dtype dt,
+                                  int B, int S, int h, int D, const int32_t *kv_nb,
+                                  const int32_t *kv_inds, float scale, void *o, float *lse,
+                                  nabla_stream_t stream) {
   using namespace nabla;
   if (!valid_shape(B, S, h, D) || !valid_dtype(dt)) return NABLA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return NABLA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !kv_nb || !kv_inds) return NABLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
-      !aligned(kv_nb, 4) || !aligned(kv_inds, 4))
+      !aligned(kv_nb, 4) || !aligned(kv_inds, 4) || !aligned(lse, 4))
     return NABLA_ERR_INVALID_ARG;
   const Shape s{B, S, h, D, S / 64};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -158,10 +159,24 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
   int *status = device_status_ptr(&e);
   if (!status) return NABLA_ERR_CUDA;
   if (dt == NABLA_BF16)
-    e = launch_attn_tc(q, k, v, s, kv_nb, kv_inds, scale, o, status, st);
+    e = launch_attn_tc(q, k, v, s, kv_nb, kv_inds, scale, o, lse, status, st);
   else
-    e = launch_attn_simt(q, k, v, dt, s, kv_nb, kv_inds, scale, o, status, st);
+    e = launch_attn_simt(q, k, v, dt, s, kv_nb, kv_inds, scale, o, lse, status, st);
   return from_cuda(e);
+}
+
+nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_dtype dt, int B,
+                            int S, int h, int D, const int32_t *kv_nb, const int32_t *kv_inds,
+                            float scale, void *o, nabla_stream_t stream) {
+  return attn_fwd_call(q, k, v, dt, B, S, h, D, kv_nb, kv_inds, scale, o, nullptr, stream);
+}
+
+nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nabla_dtype dt,
+                                int B, int S, int h, int D, const int32_t *kv_nb,
+                                const int32_t *kv_inds, float scale, void *o, float *lse,
+                                nabla_stream_t stream) {
+  if (!lse) return NABLA_ERR_INVALID_ARG;
+  return attn_fwd_call(q, k, v, dt, B, S, h, D, kv_nb, kv_inds, scale, o, lse, stream);
 }
 
 size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D) {
@@ -170,7 +185,8 @@ size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D) {
 }
 
 nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                            const void *dout, nabla_dtype dt, int B, int S, int h, int D,
+                            const float *lse, const void *dout, nabla_dtype dt, int B, int S,
+                            int h, int D,
                             const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
                             void *dk, void *dv, void *workspace, size_t ws_bytes,
                             nabla_stream_t stream) {
@@ -184,7 +200,7 @@ nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const v
   for (void *p : out)
     if (!p || !aligned(p, 16)) return NABLA_ERR_INVALID_ARG;
   if (!kv_nb || !kv_inds || !workspace || !aligned(kv_nb, 4) || !aligned(kv_inds, 4) ||
-      !aligned(workspace, 256))
+      !aligned(workspace, 256) || !aligned(lse, 4))
     return NABLA_ERR_INVALID_ARG;
   const Shape s{B, S, h, D, S / 64};
   if (ws_bytes < bwd_workspace_layout(s).total) return NABLA_ERR_INVALID_ARG;
@@ -192,8 +208,8 @@ nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const v
   cudaError_t e;
   int *status = device_status_ptr(&e);
   if (!status) return NABLA_ERR_CUDA;
-  return from_cuda(launch_attn_bwd(q, k, v, o, dout, dt, s, kv_nb, kv_inds, scale, dq, dk, dv,
-                                   workspace, status, st));
+  return from_cuda(launch_attn_bwd(q, k, v, o, lse, dout, dt, s, kv_nb, kv_inds, scale, dq, dk,
+                                   dv, workspace, status, st));
 }
 
 static nabla_status fractal_call(const void *src, void *dst, bool flatten, nabla_dtype dt, int B,

@@ -27,6 +27,7 @@
 // the other operand is a broadcast.  CSR entries are checked as the forward
 // checks them (range, strictly ascending); bad ones are skipped and reported.
 #include <cfloat>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 
@@ -47,7 +48,8 @@ struct BwdArgs {
   int S, h, s1;
   float scale, scale_log2;
   const int32_t *kv_nb, *kv_inds;
-  float *lse2, *delta;        // [B, h, S]
+  const float *lse2;          // [B, h, S]: the caller's, or lse2_ws once prep wrote it
+  float *lse2_ws, *delta;     // [B, h, S]
   int32_t *qt_nb, *qt_inds;   // [B, h, s1], [B, h, s1, s1]
   uint32_t *bits;             // [B, h, s1, W]
   int words;                  // W = ceil(s1 / 32)
@@ -115,8 +117,8 @@ __device__ __forceinline__ void tile_acc(const float *M, const float *Y, int tu,
   }
 }
 
-// ---- prep: delta and the base-2 log-sum-exp of every query row
-template <typename T, int D>
+// ---- prep: delta and (kLse) the base-2 log-sum-exp of every query row
+template <typename T, int D, bool kLse>
 __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const T *__restrict__ q,
                                                             const T *__restrict__ k,
                                                             const T *__restrict__ o,
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const T *__restrict_
     a += __shfl_xor_sync(0xffffffffu, a, 2);
     if (part == 0) A.delta[srow + r] = a;
   }
+  if (!kLse) return;  // the caller passed the forward's log-sum-exp
 
   load_rows<T, D>(Qs, q + blk, row_stride);
   const size_t row_id = ((size_t)b * A.h + hh) * A.s1 + i;
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(kThreads) bwd_prep_kernel(const T *__restrict_
   if (tx == 0) {
 #pragma unroll
     for (int a = 0; a < 4; ++a)
-      A.lse2[srow + tu + 16 * a] = l[a] > 0.f ? m[a] + log2f(l[a]) : 0.f;
+      A.lse2_ws[srow + tu + 16 * a] = l[a] > 0.f ? m[a] + log2f(l[a]) : -INFINITY;
   }
 }
 
@@ -419,9 +422,9 @@ constexpr size_t dq_smem() {
 
 template <typename T, int D>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const void *o,
-                         const void *dout, const Shape &s, BwdArgs A, void *dq, void *dk,
-                         void *dv, cudaStream_t st) {
-  auto prep = bwd_prep_kernel<T, D>;
+                         const void *dout, const Shape &s, BwdArgs A, bool have_lse, void *dq,
+                         void *dk, void *dv, cudaStream_t st) {
+  auto prep = have_lse ? bwd_prep_kernel<T, D, false> : bwd_prep_kernel<T, D, true>;
   auto dkdv = bwd_dkdv_kernel<T, D>;
   auto dqk = bwd_dq_kernel<T, D>;
   cudaError_t e;
@@ -452,6 +455,9 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const void
   if ((e = launch_pdl(bwd_gather_kernel, dim3(warps_grid), dim3(kThreads), 0, st, A, rows)) !=
       cudaSuccess)
     return e;
+  if (std::is_same<T, __nv_bfloat16>::value)  // bf16: the products on the tensor cores
+    return launch_attn_bwd_tc(q, k, v, dout, s, A.kv_nb, A.kv_inds, A.qt_nb, A.qt_inds, A.lse2,
+                              A.delta, A.scale, dq, dk, dv, A.status, st);
   if ((e = launch_pdl(dkdv, grid, dim3(kThreads), dkdv_smem<D>(), st, tq, tk, tv, tdo,
                       static_cast<T *>(dk), static_cast<T *>(dv), A)) != cudaSuccess)
     return e;
@@ -477,7 +483,7 @@ BwdWorkspace bwd_workspace_layout(const Shape &s) {
 }
 
 cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                            const void *dout, nabla_dtype dt, const Shape &s,
+                            const float *lse, const void *dout, nabla_dtype dt, const Shape &s,
                             const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
                             void *dk, void *dv, void *workspace, int *status, cudaStream_t st) {
   const BwdWorkspace w = bwd_workspace_layout(s);
@@ -489,6 +495,7 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
             scale * 1.4426950408889634f,
             kv_nb,
             kv_inds,
+            lse ? lse : reinterpret_cast<const float *>(ws + w.lse2),
             reinterpret_cast<float *>(ws + w.lse2),
             reinterpret_cast<float *>(ws + w.delta),
             reinterpret_cast<int32_t *>(ws + w.qt_nb),
@@ -498,11 +505,11 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
             status};
   if (dt == NABLA_BF16) {
     if (s.D == 64)
-      return launch_typed<__nv_bfloat16, 64>(q, k, v, o, dout, s, A, dq, dk, dv, st);
-    return launch_typed<__nv_bfloat16, 128>(q, k, v, o, dout, s, A, dq, dk, dv, st);
+      return launch_typed<__nv_bfloat16, 64>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
+    return launch_typed<__nv_bfloat16, 128>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
   }
-  if (s.D == 64) return launch_typed<float, 64>(q, k, v, o, dout, s, A, dq, dk, dv, st);
-  return launch_typed<float, 128>(q, k, v, o, dout, s, A, dq, dk, dv, st);
+  if (s.D == 64) return launch_typed<float, 64>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
+  return launch_typed<float, 128>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
 }
 
 }  // namespace nabla

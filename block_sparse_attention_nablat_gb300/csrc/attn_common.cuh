@@ -1,0 +1,198 @@
+// Helpers shared by the tcgen05 attention kernels (forward and backward):
+// the pair-of-blocks work units with their entry bitmaps, packed fp32 pair
+// arithmetic, mbarrier ring positions, the in-kernel choice of the pairing
+// stride, and the TMA map of a [B, S, h, D] bf16 tensor.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace nabla {
+namespace tcattn {
+
+constexpr int kMaxWords = 64;  // s1 <= 2048 blocks -> 64 bitmap words
+
+struct UnitInfo {
+  uint32_t a[kMaxWords];  // kept by the first query block of the pair
+  uint32_t b[kMaxWords];  // kept by the second
+  int n;                  // union size
+  int pad;
+};
+
+struct Cursor {
+  int w;
+  uint32_t m;
+};
+
+__device__ __forceinline__ int next_entry(const UnitInfo &inf, Cursor &c, uint32_t &flags) {
+  while (c.m == 0u && c.w + 1 < kMaxWords) {
+    ++c.w;
+    c.m = inf.a[c.w] | inf.b[c.w];
+  }
+  const int bit = c.m ? __ffs(c.m) - 1 : 0;
+  c.m &= c.m - 1u;
+  flags = ((inf.a[c.w] >> bit) & 1u) | (((inf.b[c.w] >> bit) & 1u) << 1);
+  return c.w * 32 + bit;
+}
+
+// Query block `side` (0 or 1) of pair pr at stride d: pairs run through groups
+// of 2d consecutive blocks, (g 2d + o, g 2d + o + d) for o < d.
+__device__ __forceinline__ int pair_block(int pr, int side, int d) {
+  const int g = pr / d;
+  return 2 * g * d + (pr - g * d) + side * d;
+}
+
+struct Unit {
+  int b, hh, pr;
+};
+__device__ __forceinline__ Unit decode(long u, int npairs, int h) {
+  const long bh = u / npairs;
+  Unit r;
+  r.pr = (int)(u - bh * npairs);
+  r.b = (int)(bh / h);
+  r.hh = (int)(bh - (long)r.b * h);
+  return r;
+}
+
+// packed fp32 pairs (sm_100+ f32x2 arithmetic)
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Ring position: slot index and phase parity advanced without division.
+template <int N>
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == (uint32_t)N) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Pairing stride: the candidate d (1, or any d with 2d dividing s1) whose
+// pairs have the smallest total list union over a fixed sample of pairs.  Run
+// by all threads of every CTA (at most 12 warps) on scratch shared memory
+// before the roles start; integer counts make the choice identical in every
+// CTA.  L: any struct with B, S, h and the CSR lists kv_nb, kv_inds.
+constexpr int kMaxCands = 24, kSamples = 16;
+struct StrideScratch {
+  uint32_t bits[12][kMaxWords];
+  unsigned long long total[kMaxCands];
+  int cand[kMaxCands];
+  int ncand, chosen;
+};
+
+template <class L>
+__device__ int choose_pair_stride(const L &P, StrideScratch *sc) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
+  const long units = (long)P.B * P.h * npairs;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    sc->cand[n++] = 1;
+    for (int d = 2; 2 * d <= s1 && n < kMaxCands; ++d)
+      if (s1 % (2 * d) == 0) sc->cand[n++] = d;
+    sc->ncand = n;
+    for (int c = 0; c < kMaxCands; ++c) sc->total[c] = 0ull;
+  }
+  __syncthreads();
+  const int ncand = sc->ncand;
+  if (ncand > 1) {
+    uint32_t *bits = sc->bits[warp];
+    for (int t = warp; t < ncand * kSamples; t += (int)(blockDim.x >> 5)) {
+      const int c = t / kSamples, k = t - c * kSamples;
+      const int d = sc->cand[c];
+      // the same units for every candidate, spread over all heads and rows
+      const long u = (long)(((unsigned long long)k * 2654435761ull) % (unsigned long long)units);
+      const Unit un = decode(u, npairs, P.h);
+      const long bh = (long)un.b * P.h + un.hh;
+      int cnt[2];
+      const int32_t *list[2];
+#pragma unroll
+      for (int side = 0; side < 2; ++side) {
+        const int qb = pair_block(un.pr, side, d);
+        const size_t row = (size_t)bh * s1 + (qb < s1 ? qb : 0);
+        const int n = qb < s1 ? P.kv_nb[row] : 0;
+        cnt[side] = n < 0 ? 0 : (n > s1 ? s1 : n);
+        list[side] = P.kv_inds + row * s1;
+      }
+      for (int w = lane; w < kMaxWords; w += 32) bits[w] = 0u;
+      __syncwarp();
+      for (int n = lane; n < cnt[0]; n += 32) {
+        const int j = list[0][n];
+        if (j >= 0 && j < s1) atomicOr(&bits[j >> 5], 1u << (j & 31));
+      }
+      __syncwarp();
+      int uni = 0;  // entries of the second list not in the first
+      for (int w = lane; w < kMaxWords; w += 32) uni += __popc(bits[w]);
+      for (int n = lane; n < cnt[1]; n += 32) {
+        const int j = list[1][n];
+        if (j >= 0 && j < s1 && !((bits[j >> 5] >> (j & 31)) & 1u)) ++uni;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) uni += __shfl_xor_sync(0xffffffffu, uni, o);
+      if (lane == 0) atomicAdd(&sc->total[c], (unsigned long long)uni);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = 0;
+    for (int c = 1; c < ncand; ++c)
+      if (sc->total[c] < sc->total[best]) best = c;
+    sc->chosen = sc->cand[best];
+  }
+  __syncthreads();
+  const int d = sc->chosen;
+  __syncthreads();  // the scratch is handed back to the pipeline after this
+  return d;
+}
+
+// ---------------------------------------------------------------- host side
+// [B, S, h, D] bf16 viewed as a 4-D tensor (D, h, S, B); box = 64 columns x `rows` tokens.
+inline bool make_map(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap *m, const void *ptr,
+              const Shape &s, int rows) {
+  cuuint64_t dims[4] = {(cuuint64_t)s.D, (cuuint64_t)s.h, (cuuint64_t)s.S, (cuuint64_t)s.B};
+  cuuint64_t strides[3] = {(cuuint64_t)s.D * 2, (cuuint64_t)s.h * s.D * 2,
+                           (cuuint64_t)s.S * s.h * s.D * 2};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace tcattn
+}  // namespace nabla

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T *__restrict__ q,
                                                         const int32_t *__restrict__ kv_nb,
                                                         const int32_t *__restrict__ kv_inds,
                                                         float scale_log2, T *__restrict__ o,
-                                                        int *status) {
+                                                        float *__restrict__ lse, int *status) {
   constexpr int DQ = D / 4;
   extern __shared__ float smem[];
   float *Qs = smem;               // [64][D + 1]
@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T *__restrict__ q,
   }
 
   const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+  if (lse && part == 0)  // base-2 log-sum-exp of the row's scaled scores
+    lse[((size_t)b * h + hh) * S + (size_t)i * 64 + r] =
+        l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
   T *orow = o + head_off + (size_t)(i * 64 + r) * row_stride + part * DQ;
 #pragma unroll
   for (int e = 0; e < DQ; ++e) from_f(orow[e], acc[e] * inv);
@@ -128,7 +131,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(const T *__restrict__ q,
 template <typename T, int D>
 cudaError_t launch_typed(const void *q, const void *k, const void *v, const Shape &s,
                          const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *o,
-                         int *status, cudaStream_t st) {
+                         float *lse, int *status, cudaStream_t st) {
   const size_t smem = sizeof(float) * (64 * (D + 1) * 2 + 64 * D + 64 * 65);
   auto kern = attn_simt_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -136,20 +139,22 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const Shap
   dim3 grid(s.s1, s.h, s.B);
   return launch_pdl(kern, grid, dim3(256), smem, st, static_cast<const T *>(q),
                     static_cast<const T *>(k), static_cast<const T *>(v), s.S, s.h, kv_nb, kv_inds,
-                    scale * 1.4426950408889634f, static_cast<T *>(o), status);
+                    scale * 1.4426950408889634f, static_cast<T *>(o), lse, status);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_simt(const void *q, const void *k, const void *v, nabla_dtype dt,
                              const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,
-                             float scale, void *o, int *status, cudaStream_t st) {
+                             float scale, void *o, float *lse, int *status, cudaStream_t st) {
   if (dt == NABLA_F32)
-    return s.D == 64 ? launch_typed<float, 64>(q, k, v, s, kv_nb, kv_inds, scale, o, status, st)
-                     : launch_typed<float, 128>(q, k, v, s, kv_nb, kv_inds, scale, o, status, st);
-  return s.D == 64
-             ? launch_typed<__nv_bfloat16, 64>(q, k, v, s, kv_nb, kv_inds, scale, o, status, st)
-             : launch_typed<__nv_bfloat16, 128>(q, k, v, s, kv_nb, kv_inds, scale, o, status, st);
+    return s.D == 64
+               ? launch_typed<float, 64>(q, k, v, s, kv_nb, kv_inds, scale, o, lse, status, st)
+               : launch_typed<float, 128>(q, k, v, s, kv_nb, kv_inds, scale, o, lse, status, st);
+  return s.D == 64 ? launch_typed<__nv_bfloat16, 64>(q, k, v, s, kv_nb, kv_inds, scale, o, lse,
+                                                      status, st)
+                   : launch_typed<__nv_bfloat16, 128>(q, k, v, s, kv_nb, kv_inds, scale, o, lse,
+                                                       status, st);
 }
 
 }  // namespace nabla

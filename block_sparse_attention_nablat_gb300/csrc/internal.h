@@ -71,12 +71,19 @@ struct BwdWorkspace {
 };
 BwdWorkspace bwd_workspace_layout(const Shape &s);
 cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                            const void *dout, nabla_dtype dt, const Shape &s,
+                            const float *lse, const void *dout, nabla_dtype dt, const Shape &s,
                             const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
                             void *dk, void *dv, void *workspace, int *status, cudaStream_t st);
+// K7t: the bf16 backward's products on tcgen05 (dK, dV per key-block pair over
+// the transposed lists, then dQ per query-block pair), given lse2 and delta.
+cudaError_t launch_attn_bwd_tc(const void *q, const void *k, const void *v, const void *dout,
+                               const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,
+                               const int32_t *qt_nb, const int32_t *qt_inds, const float *lse2,
+                               const float *delta, float scale, void *dq, void *dk, void *dv,
+                               int *status, cudaStream_t st);
 // K3f: CUDA-core block-sparse attention (fp32 storage).
 cudaError_t launch_attn_simt(const void *q, const void *k, const void *v, nabla_dtype dt,
                              const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,
-                             float scale, void *o, int *status, cudaStream_t st);
+                             float scale, void *o, float *lse, int *status, cudaStream_t st);
 
 }  // namespace nabla

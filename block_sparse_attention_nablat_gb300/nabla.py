@@ -61,8 +61,11 @@ def load() -> ctypes.CDLL:
     lib.nabla_attn_bwd_workspace_bytes.restype = sz
     lib.nabla_attn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
     lib.nabla_attn_bwd.restype = i32
-    lib.nabla_attn_bwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+    lib.nabla_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
                                    ctypes.c_float, vp, vp, vp, vp, sz, vp]
+    lib.nabla_attn_fwd_lse.restype = i32
+    lib.nabla_attn_fwd_lse.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp,
+                                       ctypes.c_float, vp, vp, vp]
     lib.nabla_sta_mask.restype = i32
     lib.nabla_sta_mask.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp]
     for name in ("nabla_fractal_flatten", "nabla_fractal_unflatten"):
@@ -204,12 +207,34 @@ def nabla_attn_bwd_workspace_bytes(B: int, S: int, h: int, D: int) -> int:
     return load().nabla_attn_bwd_workspace_bytes(B, S, h, D)
 
 
+def nabla_attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb: torch.Tensor,
+                       kv_inds: torch.Tensor, scale: Optional[float] = None,
+                       o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       stream=None):
+    """nabla_attn_fwd that also returns the rows' base-2 log-sum-exp: (o, lse [B,h,S] fp32)."""
+    lib = load()
+    B, S, h, D = _shape(q)
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k, v must match q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = lib.nabla_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D,
+                                _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(o), _ptr(lse),
+                                _stream(stream))
+    _check(st, "nabla_attn_fwd_lse")
+    return o, lse
+
+
 def nabla_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor,
                    dout: torch.Tensor, kv_nb: torch.Tensor, kv_inds: torch.Tensor,
                    scale: Optional[float] = None, dq: Optional[torch.Tensor] = None,
                    dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-                   workspace: Optional[torch.Tensor] = None, stream=None):
-    """Gradients of nabla_attn_fwd: returns (dq, dk, dv), each [B,S,h,D] in q's dtype."""
+                   workspace: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Gradients of nabla_attn_fwd: returns (dq, dk, dv), each [B,S,h,D] in q's dtype.
+    lse: the forward's log-sum-exp from nabla_attn_fwd_lse (computed here if None)."""
     lib = load()
     B, S, h, D = _shape(q)
     for t in (k, v, o, dout):
@@ -223,8 +248,8 @@ def nabla_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
     need = lib.nabla_attn_bwd_workspace_bytes(B, S, h, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    st = lib.nabla_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _dtype_code(q), B, S,
-                            h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(dq), _ptr(dk),
+    st = lib.nabla_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                            _dtype_code(q), B, S, h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "nabla_attn_bwd")

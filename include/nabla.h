@@ -205,6 +205,20 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
                             float scale, void *o, nabla_stream_t stream);
 
 /*
+ * nabla_attn_fwd_lse -- nabla_attn_fwd that also writes, for every query row,
+ * the base-2 log-sum-exp of its scaled scores over the kept tokens J:
+ *   lse[(b*h + hh)*S + s] = log2( sum_{u in J} 2^(scale * log2(e) * <q_s, k_u>) ),
+ * or -INFINITY for a row whose block keeps nothing.  A training step stores it
+ * for nabla_attn_bwd, which then needs no pass of its own to renormalise P.
+ *   lse  [B, h, S] device fp32, 4-byte aligned, written (NULL is rejected).
+ * Everything else, including o, is exactly as nabla_attn_fwd.
+ */
+nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nabla_dtype dt,
+                                int B, int S, int h, int D, const int32_t *kv_nb,
+                                const int32_t *kv_inds, float scale, void *o, float *lse,
+                                nabla_stream_t stream);
+
+/*
  * nabla_attn_bwd -- gradients of nabla_attn_fwd with respect to q, k and v
  * (gist.science NABLA summary, "Dual-Phase Acceleration" and Experimental
  * Results: the method trains with the block mask, so the forward is
@@ -223,6 +237,9 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
  * step).  Arithmetic is fp32 on CUDA cores; dq, dk, dv are written in dt.
  *
  *   q, k, v, o, dout  [B, S, h, D] device, element type dt.
+ *   lse               [B, h, S] device fp32 from nabla_attn_fwd_lse for the same
+ *                     inputs, or NULL: the library then computes it (one more
+ *                     pass over the kept blocks, on CUDA cores).
  *   kv_nb, kv_inds    the mask, as for nabla_attn_fwd (bad entries are skipped
  *                     and reported as NABLA_ERR_BAD_INDEX).
  *   scale             the forward's softmax scale.
@@ -236,7 +253,8 @@ nabla_status nabla_attn_fwd(const void *q, const void *k, const void *v, nabla_d
  */
 size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D);
 nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                            const void *dout, nabla_dtype dt, int B, int S, int h, int D,
+                            const float *lse, const void *dout, nabla_dtype dt, int B, int S,
+                            int h, int D,
                             const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *dq,
                             void *dk, void *dv, void *workspace, size_t ws_bytes,
                             nabla_stream_t stream);

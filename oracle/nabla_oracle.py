@@ -244,6 +244,31 @@ def block_sparse_attention(q, k, v, kv_nb, kv_inds, scale: float,
     return out
 
 
+def attention_lse2(q, k, kv_nb, kv_inds, scale: float,
+                   qblocks: Optional[Iterable[Tuple[int, int, int]]] = None):
+    """Base-2 log-sum-exp of each query row's scaled scores over its kept tokens,
+    log2(sum_u 2^(scale log2(e) <q_s, k_u>)) = (natural log-sum-exp) / ln 2;
+    float64 [B, h, S], -inf for rows whose block keeps nothing, NaN for rows of
+    unlisted blocks."""
+    B, S, h, D = q.shape
+    s1 = S // BLOCK
+    out = np.full((B, h, S), np.nan, dtype=np.float64)
+    if qblocks is None:
+        qblocks = [(b, hh, i) for b in range(B) for hh in range(h) for i in range(s1)]
+    for b, hh, i in qblocks:
+        n = int(kv_nb[b, hh, i])
+        rows = slice(i * BLOCK, (i + 1) * BLOCK)
+        if n == 0:
+            out[b, hh, rows] = -np.inf
+            continue
+        blocks = np.asarray(kv_inds[b, hh, i, :n], dtype=np.int64)
+        tok = (blocks[:, None] * BLOCK + np.arange(BLOCK)[None, :]).ravel()
+        z = scale * (q[b, rows, hh, :].astype(np.float64) @ k[b, tok, hh, :].astype(np.float64).T)
+        m = z.max(axis=1)
+        out[b, hh, rows] = (m + np.log(np.exp(z - m[:, None]).sum(axis=1))) / math.log(2.0)
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Backward of a7 (training).  gist.science NABLA summary, "Dual-Phase
 # Acceleration" and Experimental Results (pre-training iteration time): the

@@ -132,18 +132,28 @@ def test_attn_rejects(lib, kw):
 
 
 def _bwd(lib, **kw):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, g=FAKE, dt=1, B=1, S=1024, h=2, D=64, nb=FAKE,
-             inds=FAKE, scale=0.125, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, wsb=1 << 30, st=None)
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, g=FAKE, dt=1, B=1, S=1024, h=2, D=64,
+             nb=FAKE, inds=FAKE, scale=0.125, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, wsb=1 << 30,
+             st=None)
     a.update(kw)
-    return lib.nabla_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["g"], a["dt"], a["B"], a["S"],
-                              a["h"], a["D"], a["nb"], a["inds"], a["scale"], a["dq"], a["dk"],
-                              a["dv"], a["ws"], a["wsb"], a["st"])
+    return lib.nabla_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["g"], a["dt"], a["B"],
+                              a["S"], a["h"], a["D"], a["nb"], a["inds"], a["scale"], a["dq"],
+                              a["dk"], a["dv"], a["ws"], a["wsb"], a["st"])
+
+
+def test_attn_fwd_lse_rejects(lib):
+    args = [FAKE, FAKE, FAKE, 1, 1, 1024, 2, 64, FAKE, FAKE, 0.125, FAKE]
+    assert lib.nabla_attn_fwd_lse(*args, None, None) == INVALID       # lse required
+    assert lib.nabla_attn_fwd_lse(*args, FAKE + 2, None) == INVALID   # lse misaligned
+    bad = list(args)
+    bad[5] = 1000
+    assert lib.nabla_attn_fwd_lse(*bad, FAKE, None) == INVALID
 
 
 @pytest.mark.parametrize("kw", [dict(S=1000), dict(D=32), dict(B=0), dict(o=None), dict(g=None),
                                 dict(dq=None), dict(dk=FAKE + 4), dict(dv=None), dict(ws=None),
                                 dict(ws=FAKE + 64), dict(wsb=1000), dict(nb=FAKE + 2),
-                                dict(scale=float("nan")), dict(dt=3)],
+                                dict(scale=float("nan")), dict(dt=3), dict(lse=FAKE + 2)],
                          ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
 def test_attn_bwd_rejects(lib, kw):
     assert _bwd(lib, **kw) == INVALID

@@ -4,9 +4,11 @@ The mask comes from the GPU mask builder and o from the GPU forward (what a
 training step stores); the oracle gets the same mask and the same o (reading
 R17).  Tolerances, derived from the arithmetic (the pages fix none for the
 backward): fp32 storage, max|err| <= 1e-4 * max|ref| per gradient (fp32 sums
-of up to ~10^5 terms); bf16 storage, the gradients are rounded to bf16
-(relative 2^-9 per element): max|err| <= 1e-2 * max|ref| and
-mean|err| <= 2e-3 * mean|ref|.  At full size the checks are the invariants
+of up to ~10^5 terms); bf16 storage, P and dz are rounded to bf16 before the
+tensor-core products (as the forward rounds P, reading R9) and the gradients
+are rounded to bf16: dz sums to zero along a row, so dq and dk are sums with
+cancellation and carry about 2^-8 of relative error on average:
+max|err| <= 2e-2 * max|ref| and mean|err| <= 5e-3 * mean|ref|.  At full size the checks are the invariants
 sum_u dk_u = 0 and sum_u dv_u = sum of dout over rows that keep something,
 plus exact oracle values on sampled blocks.
 """
@@ -20,7 +22,7 @@ from oracle import nabla_oracle as O
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-TOL = {"f32": (1e-4, None), "bf16": (1e-2, 2e-3)}
+TOL = {"f32": (1e-4, None), "bf16": (2e-2, 5e-3)}
 
 
 @pytest.fixture(scope="module")
@@ -65,7 +67,7 @@ def compare(w, got, ref):
         assert err.max() <= amax * scale, (name, err.max(), scale)
         if amean is not None:
             assert err.mean() <= amean * np.abs(r).mean(), (name, err.mean(), np.abs(r).mean())
-        out.append(float(err.max() / scale))
+        out.append((float(err.max() / scale), float(err.mean() / np.abs(r).mean())))
     return out
 
 
@@ -82,7 +84,7 @@ def full_check(nabla, w, seed=0, thr=None, nb=None, inds=None):
 @pytest.mark.parametrize("name", ["tiny_f32", "small_bf16"])
 def test_bwd_small_configs(nabla, name):
     rel, _ = full_check(nabla, W.WORKLOADS[name])
-    print("BWD", name, "max err / max |ref| (dq, dk, dv):", rel)
+    print("BWD", name, "(max err / max |ref|, mean err / mean |ref|) for dq, dk, dv:", rel)
 
 
 @pytest.mark.parametrize("B,h,D,s1,dtype", [(2, 3, 64, 37, "bf16"), (1, 2, 128, 10, "f32"),
@@ -143,8 +145,9 @@ def test_bwd_480p_invariants_and_sampled_blocks(nabla):
         assert np.abs(g - r).mean() <= amean * np.abs(r).mean()
 
 
-def test_bwd_bad_index_is_reported_and_skipped(nabla):
-    w = W.custom("bwd_bad", 1, 1, 64, 64 * 4, (4, 1, 1), dtype="f32")
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_bad_index_is_reported_and_skipped(nabla, dtype):
+    w = W.custom("bwd_bad", 1, 1, 64, 64 * 4, (4, 1, 1), dtype=dtype)
     keep = np.ones((1, 1, 4, 4), bool)
     nb, inds = O.csr_from_mask(keep)
     inds[0, 0, 1, 2] = 9           # out of range: skipped
@@ -153,3 +156,49 @@ def test_bwd_bad_index_is_reported_and_skipped(nabla):
     dq, dk, dv, o, *_rest, status = run_gpu(nabla, w, data, dout, nb=nb, inds=inds)
     assert status == 5  # NABLA_ERR_BAD_INDEX
     assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "tiny_f32"])
+def test_forward_lse_matches_oracle_and_feeds_the_backward(nabla, name):
+    """nabla_attn_fwd_lse: the same o as nabla_attn_fwd (bit for bit), the rows'
+    base-2 log-sum-exp within 1e-5 (absolute, on values of order 10), and a
+    backward given that lse equal to one that computes its own."""
+    w = W.WORKLOADS[name]
+    data = W.generate(w, 0)
+    dout = W.generate_dout(w, 0)
+    q, k, v = (nabla.from_storage(data[n], DEV) for n in "qkv")
+    g = nabla.from_storage(dout, DEV)
+    sta = nabla.nabla_sta_mask(*w.grid, *w.sta_half_widths, device=DEV)
+    nb, inds = nabla.nabla_build_mask(q, k, sta, w.thr[0])
+    o = nabla.nabla_attn_fwd(q, k, v, nb, inds, w.scale)
+    o2, lse = nabla.nabla_attn_fwd_lse(q, k, v, nb, inds, w.scale)
+    assert torch.equal(o, o2)
+    qf, kf = W.as_float(data["q"]), W.as_float(data["k"])
+    ref = O.attention_lse2(qf, kf, nb.cpu().numpy(), inds.cpu().numpy(), w.scale)
+    got = lse.cpu().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(fin, np.isfinite(got))
+    assert np.abs(got[fin] - ref[fin]).max() <= 1e-5 * max(1.0, np.abs(ref[fin]).max())
+    a = nabla.nabla_attn_bwd(q, k, v, o, g, nb, inds, w.scale)
+    b = nabla.nabla_attn_bwd(q, k, v, o, g, nb, inds, w.scale, lse=lse)
+    assert nabla.nabla_get_last_device_status() == 0
+    for x, y in zip(a, b):
+        xf, yf = x.float(), y.float()
+        assert (xf - yf).abs().max().item() <= 1e-2 * xf.abs().max().item()
+
+
+def test_bwd_bf16_empty_rows_and_unkept_key_blocks(nabla):
+    """The tensor-core path: a query block that keeps nothing gets dq = 0, a key
+    block that nobody keeps gets dk = dv = 0, odd block count (a pair half past
+    the end)."""
+    w = W.custom("bwd_empty_bf16", 1, 2, 128, 64 * 9, (9, 1, 1), dtype="bf16")
+    rng = np.random.default_rng(8)
+    keep = rng.random((1, 2, 9, 9)) < 0.5
+    keep[0, 0, 2] = False
+    keep[0, 1, :, 5] = False
+    keep[0, 1, 0, 1] = True
+    nb, inds = O.csr_from_mask(keep)
+    rel, (dq, dk, dv, *_rest) = full_check(nabla, w, seed=4, nb=nb, inds=inds)
+    assert np.all(dq[0, 128:192, 0] == 0.0)
+    assert np.all(dk[0, 320:384, 1] == 0.0) and np.all(dv[0, 320:384, 1] == 0.0)
+    print("BWD", w.name, rel)

@@ -134,3 +134,36 @@ def test_backward_identical_values_kill_query_and_key_gradients():
     dq, dk, dv = O.block_sparse_attention_bwd(q, k, v, dout, nb, inds, 0.5)
     assert np.abs(dq).max() < 1e-12 and np.abs(dk).max() < 1e-12
     assert np.abs(dv).max() > 0.1
+
+
+def test_lse_closed_form_and_identity():
+    rng = np.random.default_rng(6)
+    B, h, D, s1 = 1, 2, 8, 5
+    S = s1 * BLOCK
+    q, k, v = (rng.standard_normal((B, S, h, D)) for _ in range(3))
+    nb, inds = _random_csr(rng, B, h, s1, 0.5, allow_empty=True)
+    nb[0, 0, 1] = 0
+    # q = 0: every score is 0, so the sum is the number of kept tokens
+    lz = O.attention_lse2(np.zeros_like(q), k, nb, inds, 0.4)
+    for hh in range(h):
+        for i in range(s1):
+            got = lz[0, hh, 64 * i:64 * i + 64]
+            if nb[0, hh, i] == 0:
+                assert np.all(got == -np.inf)
+            else:
+                np.testing.assert_allclose(got, np.log2(64.0 * nb[0, hh, i]), rtol=1e-14)
+    # 2^(z log2(e) - lse2) are the softmax weights: they rebuild the forward's o
+    scale = 0.4
+    lse = O.attention_lse2(q, k, nb, inds, scale)
+    o = O.block_sparse_attention(q, k, v, nb, inds, scale)
+    for hh in range(h):
+        for i in range(s1):
+            n = nb[0, hh, i]
+            if n == 0:
+                continue
+            tok = (inds[0, hh, i, :n][:, None] * 64 + np.arange(64)[None, :]).ravel()
+            rows = slice(64 * i, 64 * i + 64)
+            z = scale * q[0, rows, hh] @ k[0, tok, hh].T
+            w = np.exp2(z / np.log(2.0) - lse[0, hh, rows][:, None])
+            np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-12)
+            np.testing.assert_allclose(w @ v[0, tok, hh], o[0, rows, hh], rtol=1e-10, atol=1e-12)
