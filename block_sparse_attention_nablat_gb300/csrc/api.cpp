@@ -200,7 +200,7 @@ nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const v
   for (void *p : out)
     if (!p || !aligned(p, 16)) return NABLA_ERR_INVALID_ARG;
   if (!kv_nb || !kv_inds || !workspace || !aligned(kv_nb, 4) || !aligned(kv_inds, 4) ||
-      !aligned(workspace, 256) || !aligned(lse, 4))
+      !aligned(workspace, 256) || !aligned(lse, 16))
     return NABLA_ERR_INVALID_ARG;
   const Shape s{B, S, h, D, S / 64};
   if (ws_bytes < bwd_workspace_layout(s).total) return NABLA_ERR_INVALID_ARG;

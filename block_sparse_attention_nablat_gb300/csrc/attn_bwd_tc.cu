@@ -17,15 +17,20 @@
 //    the key blocks either block kept.  A operands = the pair's q and dout
 //    rows; each step loads the entry's k and v tiles; lse2 / delta are per row.
 // A step (64 entry rows) issues two SS MMAs, X = A1 T1^T and Y = A2 T2^T
-// (M = 128, N = 64), into one of two TMEM buffer pairs.  The 128 threads of
-// warps 4-7 (thread = TMEM lane = row of the unit pair) then form
+// (M = 128, N = 64), into TMEM.  Warps 4-11 (thread = TMEM lane = row of the
+// unit pair; warps 4-7 take entry columns 0-31, warps 8-11 columns 32-63) load
+// their X and Y columns, release X / Y at once (so the next step's SS MMAs can
+// overwrite them while they compute), and form
 //   dK/dV: P^T = 2^(X sl2 - lse2[col]),  dz^T = P^T (Y - delta[col]);
 //   dQ:    P   = 2^(X sl2 - lse2[row]),  dz   = P   (Y - delta[row]);
-// with P = 0 in the rows whose block did not keep the entry.  They write P and
-// dz as bf16 over the first columns of the buffer, and TS MMAs accumulate
+// with P = 0 in the rows whose block did not keep the entry.  P and dz go as
+// bf16 into one of two P/dz buffers, and TS MMAs accumulate
 //   dK/dV: dV += P^T dout, dK += dz^T q;   dQ: dQ += dz k.
-// One thread issues every MMA, in the order SS(g), TS(g-1), so the softmax of
-// step g-1 overlaps the products of step g.  Every mbarrier wait is bounded
+// One thread issues every MMA, in the order SS(g), TS(g-1), SS(g+1), ..., so
+// the tensor pipe works on TS(g-1) and SS(g+1) while the softmax of step g
+// runs.  TMEM (512 columns): dK or dQ [0, D), dV [D, 2D), X [2D, 2D + 64),
+// Y [2D + 64, 2D + 128), P/dz buffer b at 2D + 128 + 64 b (P in its first 32
+// columns, dz in the next 32).  Every mbarrier wait is bounded
 // (1 s); on expiry the kernel records NABLA_ERR_TIMEOUT, the roles stop,
 // in-flight copies and MMAs are drained and TMEM is released.
 #include <cuda.h>
@@ -48,25 +53,25 @@ struct BCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kPairBytes = 128 * D * 2;  // A operand: 128 rows
   static constexpr int kTileBytes = 64 * D * 2;   // one 64-row tile
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 4;
   static constexpr int kStageBytes = 2 * kTileBytes + 1024;  // T1, T2, lse2 / delta (dK/dV)
   static constexpr int kOffA1 = 0;
   static constexpr int kOffA2 = kPairBytes;
   static constexpr int kOffStage = 2 * kPairBytes;
   static constexpr int kOffInfo = kOffStage + kStages * kStageBytes;
   static constexpr int kOffBars = kOffInfo + 2 * (int)sizeof(UnitInfo);
-  // TMEM: acc1 (dK or dQ) [0, D), acc0 (dV) [D, 2D), buffer b: X at 2D + 128 b, Y at +64
-  static constexpr uint32_t kAcc1 = 0, kAcc0 = D, kBuf = 2 * D;
+  static constexpr uint32_t kAcc1 = 0, kAcc0 = D, kX = 2 * D, kY = 2 * D + 64, kPD = 2 * D + 128;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdSS = idesc_bf16(128, 64, 0, 0);
   static constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 384;
+  static constexpr int kSoftmax = 256;  // threads of warps 4-11
 };
 
 struct BSync {
-  uint64_t st_full[3], st_empty[3];
+  uint64_t st_full[4], st_empty[4];
   uint64_t a_full, a_empty, info_full[2], info_empty[2];
-  uint64_t s_full[2], p_full[2], buf_free[2];
+  uint64_t s_full, x_read, p_full[2], pd_free[2];
   uint64_t acc_full, acc_free, drain;
   uint32_t tmem_slot;
   int abort;
@@ -182,18 +187,13 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
       uint32_t fl;
       const int j = next_entry(inf, cur, fl);
       uint8_t *stage = smem + C::kOffStage + st * C::kStageBytes;
-      if (!kDQ) {  // the entry's 64 lse2 / delta values, two of each per lane
-        float *ld = reinterpret_cast<float *>(stage + 2 * C::kTileBytes);
-        const size_t at = (size_t)bh * P.S + (size_t)j * 64 + 2 * lane;
-        ld[2 * lane] = P.lse2[at];
-        ld[2 * lane + 1] = P.lse2[at + 1];
-        ld[64 + 2 * lane] = P.delta[at];
-        ld[64 + 2 * lane + 1] = P.delta[at + 1];
-        __threadfence_block();
-      }
-      __syncwarp();  // the plain stores above come before lane 0's arrive
       if (lane == 0) {
-        mbar_expect_tx(&sy->st_full[st], 2 * C::kTileBytes);
+        mbar_expect_tx(&sy->st_full[st], 2 * C::kTileBytes + (kDQ ? 0 : 512));
+        if (!kDQ) {  // the entry's 64 lse2 and 64 delta values (16-byte aligned rows)
+          const size_t at = (size_t)bh * P.S + (size_t)j * 64;
+          bulk_load(stage + 2 * C::kTileBytes, P.lse2 + at, 256, &sy->st_full[st]);
+          bulk_load(stage + 2 * C::kTileBytes + 256, P.delta + at, 256, &sy->st_full[st]);
+        }
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c) {
           tma_load_4d(stage + c * 64 * 128, mT1, &sy->st_full[st], c * 64, un.hh, j * 64, un.b);
@@ -211,8 +211,8 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
   }
 }
 
-// Warp 1, lane 0: every MMA.  SS(g) for step g, then TS(g-1) once the
-// softmax of step g-1 has written its P / dz.
+// Warp 1, lane 0: every MMA.  SS(g) once the softmax of step g-1 has read
+// X and Y, then TS(g-1) once it has written its P / dz.
 template <int D, bool kDQ>
 __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy, uint32_t tmem,
                       volatile int *abort) {
@@ -234,18 +234,18 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
         !mbar_wait(&sy->acc_free, (ku - 1) & 1u, abort, P.status, kDevTimeout))
       return false;
     tc_fence_after();
-    const uint32_t xb = tmem + C::kBuf + b * 128;
+    const uint32_t pd = tmem + C::kPD + b * 64;
     const uint64_t t1 = tm_desc + (uint64_t)((st * C::kStageBytes) >> 4);
     const uint64_t t2 = tm_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
       const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
       const uint32_t acc = (ee > 0 || kk > 0) ? 1u : 0u;
-      if (!kDQ) mma_ts(tmem + C::kAcc0, xb + kk * 8, t2 + dk, C::kIdTS, acc);  // dV += P^T dout
-      mma_ts(tmem + C::kAcc1, xb + 64 + kk * 8, t1 + dk, C::kIdTS, acc);      // dK / dQ
+      if (!kDQ) mma_ts(tmem + C::kAcc0, pd + kk * 8, t2 + dk, C::kIdTS, acc);  // dV += P^T dout
+      mma_ts(tmem + C::kAcc1, pd + 32 + kk * 8, t1 + dk, C::kIdTS, acc);      // dK / dQ
     }
     mma_commit(&sy->st_empty[st]);
-    mma_commit(&sy->buf_free[b]);
+    mma_commit(&sy->pd_free[b]);
     return true;
   };
   for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
@@ -256,23 +256,22 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
       if (!mbar_wait(&sy->a_full, ka & 1u, abort, P.status, kDevTimeout)) break;
       uint32_t prev_st = 0;
       for (int e = 0; e < n; ++e, ++g, ++ge) {
-        const uint32_t st = ge % C::kStages, b = g & 1u;
+        const uint32_t st = ge % C::kStages;
         ok = mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u, abort, P.status, kDevTimeout);
-        if (ok && g >= 2)
-          ok = mbar_wait(&sy->buf_free[b], ((g >> 1) - 1) & 1u, abort, P.status, kDevTimeout);
+        if (ok && g >= 1)  // the softmax of step g-1 has read X and Y
+          ok = mbar_wait(&sy->x_read, (g - 1) & 1u, abort, P.status, kDevTimeout);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t xb = tmem + C::kBuf + b * 128;
         const uint64_t t1 = tk_desc + (uint64_t)((st * C::kStageBytes) >> 4);
         const uint64_t t2 = tk_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t da = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
           const uint64_t dt = (uint64_t)((((kk >> 2) * 64 * 128) + (kk & 3) * 32) >> 4);
-          mma_ss(xb, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);       // X = A1 T1^T
-          mma_ss(xb + 64, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // Y = A2 T2^T
+          mma_ss(tmem + C::kX, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // A1 T1^T
+          mma_ss(tmem + C::kY, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // A2 T2^T
         }
-        mma_commit(&sy->s_full[b]);
+        mma_commit(&sy->s_full);
         if (e > 0 && !(ok = ts(g - 1, e - 1, prev_st))) break;
         prev_st = st;
       }
@@ -290,12 +289,13 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
 }
 
 // 32 columns of P and dz from X and Y (fp32 in registers), stored as bf16 over
-// 16 TMEM columns each.  lse / dl: per column (dK/dV) or the row's (dQ).
+// 16 TMEM columns each (P at paddr, dz at daddr).  lse / dl: per column (dK/dV)
+// or the row's (dQ).
 template <bool kDQ>
 __device__ __forceinline__ void form_pd(const uint32_t (&x)[32], const uint32_t (&y)[32],
                                         const float *lse_c, const float *dl_c, float lse_r,
-                                        float dl_r, float sl2, bool act, uint32_t xaddr,
-                                        uint32_t yaddr) {
+                                        float dl_r, float sl2, bool act, uint32_t paddr,
+                                        uint32_t daddr) {
   uint32_t pk[16], dk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -311,16 +311,19 @@ __device__ __forceinline__ void form_pd(const uint32_t (&x)[32], const uint32_t 
     pk[i] = pack_bf16x2(p0, p1);
     dk[i] = pack_bf16x2(d0, d1);
   }
-  if (!kDQ) tmem_st16(xaddr, pk);
-  tmem_st16(yaddr, dk);
+  if (!kDQ) tmem_st16(paddr, pk);
+  tmem_st16(daddr, dk);
 }
 
-// Warps 4-7: P and dz of every step, then the unit's gradient rows.
+// Warps 4-11: P and dz of every step (group grp = entry columns 32 grp ..
+// 32 grp + 31), then the unit's gradient rows (group grp writes half of the D
+// columns).
 template <int D, bool kDQ>
 __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy,
                           uint32_t tmem, volatile int *abort) {
   using C = BCfg<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = (warp - 4) >> 2;
   const int q4 = warp & 3;
   const int row = q4 * 32 + lane;
   const int side = row >> 6;
@@ -351,28 +354,31 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
       next_entry(info[ub], cur, fl);
       const bool act = ((fl >> side) & 1u) != 0u;
       live = __all_sync(0xffffffffu,
-                        mbar_wait(&sy->s_full[b], (g >> 1) & 1u, abort, P.status, kDevTimeout));
-      if (!kDQ && live)  // the stage's lse2 / delta (plain stores of the producer)
+                        mbar_wait(&sy->s_full, g & 1u, abort, P.status, kDevTimeout));
+      if (!kDQ && live)  // the stage's lse2 / delta (bulk copies on st_full)
         live = __all_sync(0xffffffffu, mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u,
                                                  abort, P.status, kDevTimeout));
       if (!live) break;
       tc_fence_after();
+      uint32_t x[32], y[32];
+      tmem_ld32(tmem + lane_base + C::kX + grp * 32, x);
+      tmem_ld32(tmem + lane_base + C::kY + grp * 32, y);
+      tmem_wait_ld();
+      reg_fence(x);
+      reg_fence(y);
+      tc_fence_before();
+      mbar_arrive(&sy->x_read);  // X and Y may be overwritten by the next step's products
+      // the P/dz buffer of step g was last read by the TS MMAs of step g - 2
+      if (g >= 2)
+        live = __all_sync(0xffffffffu, mbar_wait(&sy->pd_free[b], ((g >> 1) - 1) & 1u, abort,
+                                                 P.status, kDevTimeout));
+      if (!live) break;
+      tc_fence_after();
       const float *ld = reinterpret_cast<const float *>(smem + C::kOffStage + st * C::kStageBytes +
                                                         2 * C::kTileBytes);
-      const uint32_t xb = tmem + lane_base + C::kBuf + b * 128;
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {  // 32 entry columns at a time
-        uint32_t x[32], y[32];
-        tmem_ld32(xb + hf * 32, x);
-        tmem_ld32(xb + 64 + hf * 32, y);
-        tmem_wait_ld();
-        reg_fence(x);
-        reg_fence(y);
-        // P (bf16) over X columns [16 hf, 16 hf + 16), dz over Y's: both below the
-        // columns still to be read
-        form_pd<kDQ>(x, y, ld + hf * 32, ld + 64 + hf * 32, lse_r, dl_r, sl2, act,
-                     xb + hf * 16, xb + 64 + hf * 16);
-      }
+      const uint32_t pd = tmem + lane_base + C::kPD + b * 64;
+      form_pd<kDQ>(x, y, ld + grp * 32, ld + 64 + grp * 32, lse_r, dl_r, sl2, act,
+                   pd + grp * 16, pd + 32 + grp * 16);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sy->p_full[b]);
@@ -394,7 +400,8 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
       const float mul = which ? 1.0f : P.scale;
       const uint32_t col = which ? C::kAcc0 : C::kAcc1;
 #pragma unroll 1
-      for (int c = 0; c < D / 16; ++c) {
+      for (int cc = 0; cc < D / 32; ++cc) {
+        const int c = grp * (D / 32) + cc;  // this group's 16-column pieces
         uint32_t t[16];
         if (n > 0) {
           tmem_ld16(tmem + lane_base + col + c * 16, t);
@@ -426,7 +433,7 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
 }
 
 template <int D, bool kDQ>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap mA1,
                        const __grid_constant__ CUtensorMap mA2,
                        const __grid_constant__ CUtensorMap mT1,
@@ -449,13 +456,14 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&sy->a_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sy->info_full[i], 1);
-      mbar_init(&sy->info_empty[i], 128 + 1);  // softmax threads + the MMA issuer
-      mbar_init(&sy->s_full[i], 1);
-      mbar_init(&sy->p_full[i], 128);
-      mbar_init(&sy->buf_free[i], 1);
+      mbar_init(&sy->info_empty[i], C::kSoftmax + 1);  // softmax threads + the MMA issuer
+      mbar_init(&sy->p_full[i], C::kSoftmax);
+      mbar_init(&sy->pd_free[i], 1);
     }
+    mbar_init(&sy->s_full, 1);
+    mbar_init(&sy->x_read, C::kSoftmax);
     mbar_init(&sy->acc_full, 1);
-    mbar_init(&sy->acc_free, 128);
+    mbar_init(&sy->acc_free, C::kSoftmax);
     mbar_init(&sy->drain, 1);
     sy->abort = 0;
     tma_prefetch_desc(&mA1);

@@ -237,9 +237,10 @@ nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nab
  * step).  Arithmetic is fp32 on CUDA cores; dq, dk, dv are written in dt.
  *
  *   q, k, v, o, dout  [B, S, h, D] device, element type dt.
- *   lse               [B, h, S] device fp32 from nabla_attn_fwd_lse for the same
- *                     inputs, or NULL: the library then computes it (one more
- *                     pass over the kept blocks, on CUDA cores).
+ *   lse               [B, h, S] device fp32 (16-byte aligned) from
+ *                     nabla_attn_fwd_lse for the same inputs, or NULL: the
+ *                     library then computes it (one more pass over the kept
+ *                     blocks, on CUDA cores).
  *   kv_nb, kv_inds    the mask, as for nabla_attn_fwd (bad entries are skipped
  *                     and reported as NABLA_ERR_BAD_INDEX).
  *   scale             the forward's softmax scale.
@@ -249,7 +250,8 @@ nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nab
  *                     the transposed mask (for each key block, the query
  *                     blocks that kept it).
  * Errors: NABLA_ERR_INVALID_ARG as for nabla_attn_fwd, for NULL or unaligned
- * o, dout, dq, dk, dv or workspace, and for a short workspace.
+ * o, dout, dq, dk, dv or workspace, an lse not 16-byte aligned, and a short
+ * workspace.
  */
 size_t nabla_attn_bwd_workspace_bytes(int B, int S, int h, int D);
 nabla_status nabla_attn_bwd(const void *q, const void *k, const void *v, const void *o,

@@ -153,7 +153,7 @@ def test_attn_fwd_lse_rejects(lib):
 @pytest.mark.parametrize("kw", [dict(S=1000), dict(D=32), dict(B=0), dict(o=None), dict(g=None),
                                 dict(dq=None), dict(dk=FAKE + 4), dict(dv=None), dict(ws=None),
                                 dict(ws=FAKE + 64), dict(wsb=1000), dict(nb=FAKE + 2),
-                                dict(scale=float("nan")), dict(dt=3), dict(lse=FAKE + 2)],
+                                dict(scale=float("nan")), dict(dt=3), dict(lse=FAKE + 2), dict(lse=FAKE + 8)],
                          ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
 def test_attn_bwd_rejects(lib, kw):
     assert _bwd(lib, **kw) == INVALID
