@@ -102,7 +102,7 @@ struct Ring {
 
 // Pairing stride: the candidate d (1, or any d with 2d dividing s1) whose
 // pairs have the smallest total list union over a fixed sample of pairs.  Run
-// by all threads of every CTA (at most 12 warps) on scratch shared memory
+// by all threads of every CTA (the first 12 warps do the counting) on scratch shared memory
 // before the roles start; integer counts make the choice identical in every
 // CTA.  L: any struct with B, S, h and the CSR lists kv_nb, kv_inds.
 constexpr int kMaxCands = 24, kSamples = 16;
@@ -129,8 +129,10 @@ __device__ int choose_pair_stride(const L &P, StrideScratch *sc) {
   __syncthreads();
   const int ncand = sc->ncand;
   if (ncand > 1) {
-    uint32_t *bits = sc->bits[warp];
-    for (int t = warp; t < ncand * kSamples; t += (int)(blockDim.x >> 5)) {
+    // at most 12 warps take part (one scratch row each); the others skip to the barrier
+    const int nw = (int)(blockDim.x >> 5) < 12 ? (int)(blockDim.x >> 5) : 12;
+    uint32_t *bits = sc->bits[warp < 12 ? warp : 0];
+    for (int t = warp; warp < nw && t < ncand * kSamples; t += nw) {
       const int c = t / kSamples, k = t - c * kSamples;
       const int d = sc->cand[c];
       // the same units for every candidate, spread over all heads and rows
