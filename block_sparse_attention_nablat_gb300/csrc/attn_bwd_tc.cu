@@ -17,20 +17,26 @@
 //    the key blocks either block kept.  A operands = the pair's q and dout
 //    rows; each step loads the entry's k and v tiles; lse2 / delta are per row.
 // A step (64 entry rows) issues two SS MMAs, X = A1 T1^T and Y = A2 T2^T
-// (M = 128, N = 64), into TMEM.  Warps 4-11 (thread = TMEM lane = row of the
-// unit pair; warps 4-7 take entry columns 0-31, warps 8-11 columns 32-63) load
-// their X and Y columns, release X / Y at once (so the next step's SS MMAs can
-// overwrite them while they compute), and form
+// (M = 128, N = 64), into one of two TMEM buffers.  Warps 4-11 (thread = TMEM
+// lane = row of the unit pair; warps 4-7 take entry columns 0-31, warps 8-11
+// columns 32-63) load their X and Y columns and form
 //   dK/dV: P^T = 2^(X sl2 - lse2[col]),  dz^T = P^T (Y - delta[col]);
 //   dQ:    P   = 2^(X sl2 - lse2[row]),  dz   = P   (Y - delta[row]);
-// with P = 0 in the rows whose block did not keep the entry.  P and dz go as
-// bf16 into one of two P/dz buffers, and TS MMAs accumulate
+// with P = 0 in the rows whose block did not keep the entry.  P and dz are
+// stored as bf16 and TS MMAs accumulate
 //   dK/dV: dV += P^T dout, dK += dz^T q;   dQ: dQ += dz k.
-// One thread issues every MMA, in the order SS(g), TS(g-1), SS(g+1), ..., so
-// the tensor pipe works on TS(g-1) and SS(g+1) while the softmax of step g
-// runs.  TMEM (512 columns): dK or dQ [0, D), dV [D, 2D), X [2D, 2D + 64),
-// Y [2D + 64, 2D + 128), P/dz buffer b at 2D + 128 + 64 b (P in its first 32
-// columns, dz in the next 32).  Every mbarrier wait is bounded
+// One thread issues every MMA, in the order SS(g), TS(g-1), SS(g+1), ...; with
+// two X / Y buffers, SS(g+1) depends on step g-1 only, so the tensor pipe works
+// on TS(g-1) and SS(g+1) while the softmax of step g runs.  TMEM (512
+// columns):
+//   dK/dV: dK [0, D), dV [D, 2D), buffer b at 2D + 128 b (X in its first 64
+//          columns, Y in the next 64).  P and dz are written in place over the
+//          columns each group has read (group g: P at X + 32 g, dz at Y + 32 g,
+//          16 columns each), and SS(g+2) waits until TS(g) has read them;
+//   dQ:    dQ [0, D), buffer b at D + 128 b, dz buffer b at D + 256 + 64 b; the
+//          softmax releases X / Y as soon as it has loaded them, and writes dz
+//          once TS(g-2) has read the dz buffer.
+// Every mbarrier wait is bounded
 // (1 s); on expiry the kernel records NABLA_ERR_TIMEOUT, the roles stop,
 // in-flight copies and MMAs are drained and TMEM is released.
 #include <cuda.h>
@@ -48,7 +54,7 @@ namespace {
 using namespace tc;
 using namespace tcattn;
 
-template <int D>
+template <int D, bool kDQ>
 struct BCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kPairBytes = 128 * D * 2;  // A operand: 128 rows
@@ -60,18 +66,22 @@ struct BCfg {
   static constexpr int kOffStage = 2 * kPairBytes;
   static constexpr int kOffInfo = kOffStage + kStages * kStageBytes;
   static constexpr int kOffBars = kOffInfo + 2 * (int)sizeof(UnitInfo);
-  static constexpr uint32_t kAcc1 = 0, kAcc0 = D, kX = 2 * D, kY = 2 * D + 64, kPD = 2 * D + 128;
+  static constexpr uint32_t kAcc1 = 0, kAcc0 = D;
+  static constexpr uint32_t kXY = kDQ ? D : 2 * D;  // X / Y buffer b at kXY + 128 b
+  static constexpr uint32_t kPD = D + 256;          // dQ: dz buffer b at kPD + 64 b
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdSS = idesc_bf16(128, 64, 0, 0);
   static constexpr uint32_t kIdTS = idesc_bf16(128, D, 0, 1);
   static constexpr int kThreads = 384;
   static constexpr int kSoftmax = 256;  // threads of warps 4-11
+  static_assert(kXY + 256 <= kTmemCols && (!kDQ || kPD + 128 <= kTmemCols), "TMEM budget");
 };
 
 struct BSync {
   uint64_t st_full[4], st_empty[4];
   uint64_t a_full, a_empty, info_full[2], info_empty[2];
-  uint64_t s_full, x_read, p_full[2], pd_free[2];
+  uint64_t s_full[2], x_read[2], p_full[2], buf_free[2];  // buf_free: dz buffer (dQ) or
+                                                          // X / Y buffer (dK/dV) read by TS
   uint64_t acc_full, acc_free, drain;
   uint32_t tmem_slot;
   int abort;
@@ -79,11 +89,11 @@ struct BSync {
 
 template <int D>
 constexpr int bwd_smem_bytes() {
-  return 1024 + BCfg<D>::kOffBars + (int)sizeof(BSync);
+  return 1024 + BCfg<D, false>::kOffBars + (int)sizeof(BSync);
 }
 static_assert(bwd_smem_bytes<128>() <= 232448, "shared memory budget (D=128)");
-static_assert(BCfg<128>::kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
-static_assert(BCfg<64>::kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+static_assert(BCfg<128, false>::kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
+static_assert(BCfg<64, false>::kStageBytes % 1024 == 0, "stages stay 1024-byte aligned");
 
 struct TcParams {
   __nv_bfloat16 *out1, *out0;      // dK/dV mode: dK, dV; dQ mode: dQ, null
@@ -101,7 +111,7 @@ template <int D, bool kDQ>
 __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUtensorMap *mA2,
                            const CUtensorMap *mT1, const CUtensorMap *mT2, uint8_t *smem,
                            UnitInfo *info, BSync *sy, volatile int *abort) {
-  using C = BCfg<D>;
+  using C = BCfg<D, kDQ>;
   const int lane = threadIdx.x & 31;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1, words = (s1 + 31) >> 5;
   const long units = (long)P.B * P.h * npairs;
@@ -216,7 +226,7 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
 template <int D, bool kDQ>
 __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy, uint32_t tmem,
                       volatile int *abort) {
-  using C = BCfg<D>;
+  using C = BCfg<D, kDQ>;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   const uint64_t a1_desc = smem_desc_sw128(smem_u32(smem + C::kOffA1), 16, 1024);
@@ -234,18 +244,22 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
         !mbar_wait(&sy->acc_free, (ku - 1) & 1u, abort, P.status, kDevTimeout))
       return false;
     tc_fence_after();
-    const uint32_t pd = tmem + C::kPD + b * 64;
     const uint64_t t1 = tm_desc + (uint64_t)((st * C::kStageBytes) >> 4);
     const uint64_t t2 = tm_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
       const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
       const uint32_t acc = (ee > 0 || kk > 0) ? 1u : 0u;
-      if (!kDQ) mma_ts(tmem + C::kAcc0, pd + kk * 8, t2 + dk, C::kIdTS, acc);  // dV += P^T dout
-      mma_ts(tmem + C::kAcc1, pd + 32 + kk * 8, t1 + dk, C::kIdTS, acc);      // dK / dQ
+      if (kDQ) {
+        mma_ts(tmem + C::kAcc1, tmem + C::kPD + b * 64 + kk * 8, t1 + dk, C::kIdTS, acc);
+      } else {  // entries 32 g .. 32 g + 31 sit at columns 32 g .. 32 g + 15 of X and Y
+        const uint32_t xb = tmem + C::kXY + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+        mma_ts(tmem + C::kAcc0, xb, t2 + dk, C::kIdTS, acc);       // dV += P^T dout
+        mma_ts(tmem + C::kAcc1, xb + 64, t1 + dk, C::kIdTS, acc);  // dK += dz^T q
+      }
     }
     mma_commit(&sy->st_empty[st]);
-    mma_commit(&sy->pd_free[b]);
+    mma_commit(&sy->buf_free[b]);
     return true;
   };
   for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
@@ -257,9 +271,11 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
       uint32_t prev_st = 0;
       for (int e = 0; e < n; ++e, ++g, ++ge) {
         const uint32_t st = ge % C::kStages;
+        const uint32_t b = g & 1u;
         ok = mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u, abort, P.status, kDevTimeout);
-        if (ok && g >= 1)  // the softmax of step g-1 has read X and Y
-          ok = mbar_wait(&sy->x_read, (g - 1) & 1u, abort, P.status, kDevTimeout);
+        if (ok && g >= 2)  // buffer b is free: step g-2 has read X / Y (dQ), or TS(g-2)
+          ok = mbar_wait(kDQ ? &sy->x_read[b] : &sy->buf_free[b], ((g >> 1) - 1) & 1u, abort,
+                         P.status, kDevTimeout);  // has read the P / dz written over them
         if (!ok) break;
         tc_fence_after();
         const uint64_t t1 = tk_desc + (uint64_t)((st * C::kStageBytes) >> 4);
@@ -268,10 +284,11 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t da = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
           const uint64_t dt = (uint64_t)((((kk >> 2) * 64 * 128) + (kk & 3) * 32) >> 4);
-          mma_ss(tmem + C::kX, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // A1 T1^T
-          mma_ss(tmem + C::kY, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // A2 T2^T
+          const uint32_t xb = tmem + C::kXY + b * 128;
+          mma_ss(xb, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);       // X = A1 T1^T
+          mma_ss(xb + 64, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // Y = A2 T2^T
         }
-        mma_commit(&sy->s_full);
+        mma_commit(&sy->s_full[b]);
         if (e > 0 && !(ok = ts(g - 1, e - 1, prev_st))) break;
         prev_st = st;
       }
@@ -321,7 +338,7 @@ __device__ __forceinline__ void form_pd(const uint32_t (&x)[32], const uint32_t 
 template <int D, bool kDQ>
 __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy,
                           uint32_t tmem, volatile int *abort) {
-  using C = BCfg<D>;
+  using C = BCfg<D, kDQ>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = (warp - 4) >> 2;
   const int q4 = warp & 3;
@@ -354,31 +371,36 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
       next_entry(info[ub], cur, fl);
       const bool act = ((fl >> side) & 1u) != 0u;
       live = __all_sync(0xffffffffu,
-                        mbar_wait(&sy->s_full, g & 1u, abort, P.status, kDevTimeout));
+                        mbar_wait(&sy->s_full[b], (g >> 1) & 1u, abort, P.status, kDevTimeout));
       if (!kDQ && live)  // the stage's lse2 / delta (bulk copies on st_full)
         live = __all_sync(0xffffffffu, mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u,
                                                  abort, P.status, kDevTimeout));
       if (!live) break;
       tc_fence_after();
       uint32_t x[32], y[32];
-      tmem_ld32(tmem + lane_base + C::kX + grp * 32, x);
-      tmem_ld32(tmem + lane_base + C::kY + grp * 32, y);
+      const uint32_t xb = tmem + lane_base + C::kXY + b * 128;
+      tmem_ld32(xb + grp * 32, x);
+      tmem_ld32(xb + 64 + grp * 32, y);
       tmem_wait_ld();
       reg_fence(x);
       reg_fence(y);
-      tc_fence_before();
-      mbar_arrive(&sy->x_read);  // X and Y may be overwritten by the next step's products
-      // the P/dz buffer of step g was last read by the TS MMAs of step g - 2
-      if (g >= 2)
-        live = __all_sync(0xffffffffu, mbar_wait(&sy->pd_free[b], ((g >> 1) - 1) & 1u, abort,
-                                                 P.status, kDevTimeout));
-      if (!live) break;
-      tc_fence_after();
       const float *ld = reinterpret_cast<const float *>(smem + C::kOffStage + st * C::kStageBytes +
                                                         2 * C::kTileBytes);
-      const uint32_t pd = tmem + lane_base + C::kPD + b * 64;
-      form_pd<kDQ>(x, y, ld + grp * 32, ld + 64 + grp * 32, lse_r, dl_r, sl2, act,
-                   pd + grp * 16, pd + 32 + grp * 16);
+      if (kDQ) {
+        tc_fence_before();
+        mbar_arrive(&sy->x_read[b]);  // buffer b may take the products of step g + 2
+        // the dz buffer of step g was last read by the TS MMAs of step g - 2
+        if (g >= 2)
+          live = __all_sync(0xffffffffu, mbar_wait(&sy->buf_free[b], ((g >> 1) - 1) & 1u, abort,
+                                                   P.status, kDevTimeout));
+        if (!live) break;
+        tc_fence_after();
+        const uint32_t pd = tmem + lane_base + C::kPD + b * 64;
+        form_pd<kDQ>(x, y, ld, ld + 64, lse_r, dl_r, sl2, act, pd + grp * 16, pd + grp * 16);
+      } else {  // in place over the 32 columns of X and Y this thread has just read
+        form_pd<kDQ>(x, y, ld + grp * 32, ld + 64 + grp * 32, lse_r, dl_r, sl2, act,
+                     xb + grp * 32, xb + 64 + grp * 32);
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&sy->p_full[b]);
@@ -438,7 +460,7 @@ __global__ void __launch_bounds__(384, 1)
                        const __grid_constant__ CUtensorMap mA2,
                        const __grid_constant__ CUtensorMap mT1,
                        const __grid_constant__ CUtensorMap mT2, TcParams P) {
-  using C = BCfg<D>;
+  using C = BCfg<D, kDQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -458,10 +480,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sy->info_full[i], 1);
       mbar_init(&sy->info_empty[i], C::kSoftmax + 1);  // softmax threads + the MMA issuer
       mbar_init(&sy->p_full[i], C::kSoftmax);
-      mbar_init(&sy->pd_free[i], 1);
+      mbar_init(&sy->buf_free[i], 1);
+      mbar_init(&sy->s_full[i], 1);
+      mbar_init(&sy->x_read[i], C::kSoftmax);
     }
-    mbar_init(&sy->s_full, 1);
-    mbar_init(&sy->x_read, C::kSoftmax);
     mbar_init(&sy->acc_full, 1);
     mbar_init(&sy->acc_free, C::kSoftmax);
     mbar_init(&sy->drain, 1);
@@ -502,7 +524,7 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, bool kDQ>
 cudaError_t launch_mode(const void *a1, const void *a2, const void *t1, const void *t2,
                         const Shape &s, TcParams p, cudaStream_t st) {
-  using C = BCfg<D>;
+  using C = BCfg<D, kDQ>;
   cudaError_t err;
   auto enc = tensor_map_encoder(&err);
   if (!enc) return err;
