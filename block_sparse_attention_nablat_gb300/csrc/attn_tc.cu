@@ -608,9 +608,11 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
       for (int i = 0; i < 8; ++i)
         w[i] = pack_bf16x2(__uint_as_float(t[2 * i]) * inv, __uint_as_float(t[2 * i + 1]) * inv);
       if (live && row_valid) {
+        // streaming stores: o is not read again here, so its lines should not
+        // linger dirty in L2 for the next kernel to write back
         uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 16);
-        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        __stcs(dst, make_uint4(w[0], w[1], w[2], w[3]));
+        __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
       }
     }
     tc_fence_before();
