@@ -54,7 +54,7 @@ typedef struct CUstream_st *nabla_stream_t;
 typedef enum {
   NABLA_OK = 0,
   NABLA_ERR_INVALID_ARG = 1, /* bad shape, dtype, threshold, pointer or size */
-  NABLA_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. no sm_103 device) */
+  NABLA_ERR_UNSUPPORTED = 2, /* valid request this library cannot serve (e.g. no sm_103 device) */
   NABLA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
   NABLA_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up */
   NABLA_ERR_BAD_INDEX = 5    /* kv_nb / kv_inds held an out-of-range entry (skipped) */

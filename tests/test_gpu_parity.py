@@ -1,6 +1,6 @@
 """CUDA path vs the fp64 oracle, through the C ABI (needs an sm_103 GPU).
 
-Tolerances (fixed by the benchmark spec, not by the pages):
+Tolerances (the pages state none; these are the bounds this repository holds its kernels to):
   mask: kv_nb / kv_inds bit-exact except blocks whose oracle running sum lies
         within 1e-4 of 1 - thr (and that the STA does not force), and blocks in
         a near-tie straddling the cut (probabilities within a relative 1e-5, an
