@@ -19,10 +19,12 @@
 //    MMAs are spent on entries only one block of the pair needs.  Persistent
 //    CTAs (one per SM) take units round-robin in head-major order, so
 //    co-running CTAs share one head's K/V in L2.
-//  * A step covers two KV entries (128 keys).  On this hardware a tcgen05 MMA
-//    costs about 32 + N/2 cycles whatever its N, so S = Q K^T is issued with
-//    N = 128 (both entries of the step in one MMA, from a K "pair slot" whose
-//    rows 64..127 follow rows 0..63) and PV with N = D.
+//  * A step covers two KV entries (128 keys).  Measured on this hardware, a
+//    bf16 tcgen05 MMA with M = 128, K = 16 takes 48 cycles at N = 64 (two
+//    thirds of the tensor rate) and N / 2 cycles from N = 128 up (the full
+//    rate), so S = Q K^T is issued with N = 128 (both entries of the step in
+//    one MMA, from a K "pair slot" whose rows 64..127 follow rows 0..63) and PV
+//    with N = D.
 //  * TMEM: O (128 x D fp32) in columns [0, 128) and three 128-column score
 //    buffers.  With three buffers, QK^T of step s+2 only has to wait for the PV
 //    of step s-1, which is already queued ahead of PV(s), so the tensor pipe
