@@ -25,9 +25,10 @@
 // with P = 0 in the rows whose block did not keep the entry.  P and dz are
 // stored as bf16 and TS MMAs accumulate
 //   dK/dV: dV += P^T dout, dK += dz^T q;   dQ: dQ += dz k.
-// One thread issues every MMA, in the order SS(g), TS(g-1), SS(g+1), ...; with
-// two X / Y buffers, SS(g+1) depends on step g-1 only, so the tensor pipe works
-// on TS(g-1) and SS(g+1) while the softmax of step g runs.  TMEM (512
+// One thread (warp 1) issues the SS MMAs and another (warp 2) the TS MMAs, so
+// a wait in one stream never holds back the other; with two X / Y buffers,
+// SS(g+1) depends on step g-1 only, so the tensor pipe works on TS(g-1) and
+// SS(g+1) while the softmax of step g runs.  TMEM (512
 // columns):
 //   dK/dV: dK [0, D), dV [D, 2D), buffer b at 2D + 128 b (X in its first 64
 //          columns, Y in the next 64).  P and dz are written in place over the
@@ -221,61 +222,34 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
   }
 }
 
-// Warp 1, lane 0: every MMA.  SS(g) once the softmax of step g-1 has read
-// X and Y, then TS(g-1) once it has written its P / dz.
+// Warp 1, lane 0: the SS MMAs.  SS(g) once its stage has landed and buffer
+// g & 1 is free again (dQ: the softmax of step g-2 has read X / Y; dK/dV: the
+// TS MMAs of step g-2 have read the P / dz written over them).
 template <int D, bool kDQ>
-__device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy, uint32_t tmem,
-                      volatile int *abort) {
+__device__ void b_ss(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy, uint32_t tmem,
+                     volatile int *abort) {
   using C = BCfg<D, kDQ>;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   const uint64_t a1_desc = smem_desc_sw128(smem_u32(smem + C::kOffA1), 16, 1024);
   const uint64_t a2_desc = smem_desc_sw128(smem_u32(smem + C::kOffA2), 16, 1024);
   const uint64_t tk_desc = smem_desc_sw128(smem_u32(smem + C::kOffStage), 16, 1024);
-  const uint64_t tm_desc = smem_desc_sw128(smem_u32(smem + C::kOffStage), 64 * 128, 1024);
-  uint32_t g = 0, ge = 0, ka = 0, ku = 0;
+  uint32_t g = 0, ge = 0, ka = 0;
   bool ok = true;
   int k = 0;
-  // the TS MMAs of step gg (entry ee of the unit, stage st)
-  auto ts = [&](uint32_t gg, int ee, uint32_t st) -> bool {
-    const uint32_t b = gg & 1u;
-    if (!mbar_wait(&sy->p_full[b], (gg >> 1) & 1u, abort, P.status, kDevTimeout)) return false;
-    if (ee == 0 && ku > 0 &&
-        !mbar_wait(&sy->acc_free, (ku - 1) & 1u, abort, P.status, kDevTimeout))
-      return false;
-    tc_fence_after();
-    const uint64_t t1 = tm_desc + (uint64_t)((st * C::kStageBytes) >> 4);
-    const uint64_t t2 = tm_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
-      const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
-      const uint32_t acc = (ee > 0 || kk > 0) ? 1u : 0u;
-      if (kDQ) {
-        mma_ts(tmem + C::kAcc1, tmem + C::kPD + b * 64 + kk * 8, t1 + dk, C::kIdTS, acc);
-      } else {  // entries 32 g .. 32 g + 31 sit at columns 32 g .. 32 g + 15 of X and Y
-        const uint32_t xb = tmem + C::kXY + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
-        mma_ts(tmem + C::kAcc0, xb, t2 + dk, C::kIdTS, acc);       // dV += P^T dout
-        mma_ts(tmem + C::kAcc1, xb + 64, t1 + dk, C::kIdTS, acc);  // dK += dz^T q
-      }
-    }
-    mma_commit(&sy->st_empty[st]);
-    mma_commit(&sy->buf_free[b]);
-    return true;
-  };
   for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
     const int ub = k & 1;
     if (!mbar_wait(&sy->info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) break;
     const int n = info[ub].n;
     if (n > 0) {
       if (!mbar_wait(&sy->a_full, ka & 1u, abort, P.status, kDevTimeout)) break;
-      uint32_t prev_st = 0;
       for (int e = 0; e < n; ++e, ++g, ++ge) {
         const uint32_t st = ge % C::kStages;
         const uint32_t b = g & 1u;
         ok = mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u, abort, P.status, kDevTimeout);
-        if (ok && g >= 2)  // buffer b is free: step g-2 has read X / Y (dQ), or TS(g-2)
+        if (ok && g >= 2)
           ok = mbar_wait(kDQ ? &sy->x_read[b] : &sy->buf_free[b], ((g >> 1) - 1) & 1u, abort,
-                         P.status, kDevTimeout);  // has read the P / dz written over them
+                         P.status, kDevTimeout);
         if (!ok) break;
         tc_fence_after();
         const uint64_t t1 = tk_desc + (uint64_t)((st * C::kStageBytes) >> 4);
@@ -289,19 +263,70 @@ __device__ void b_mma(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *s
           mma_ss(xb + 64, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // Y = A2 T2^T
         }
         mma_commit(&sy->s_full[b]);
-        if (e > 0 && !(ok = ts(g - 1, e - 1, prev_st))) break;
-        prev_st = st;
       }
-      if (ok) ok = ts(g - 1, n - 1, prev_st);
       if (!ok) break;
-      mma_commit(&sy->a_empty);
-      mma_commit(&sy->acc_full);
+      mma_commit(&sy->a_empty);  // the unit's A rows are no longer read
       ++ka;
-      ++ku;
     }
     mbar_arrive(&sy->info_empty[ub]);
   }
   mma_commit(&sy->drain);  // never exit with MMAs in flight
+  mbar_wait(&sy->drain, 0, nullptr, P.status, kDevTimeout);
+}
+
+// Warp 2, lane 0: the TS MMAs.  TS(g) once the softmax of step g has written
+// its P / dz (and, for a unit's first step, once the epilogue has read the
+// previous unit's accumulators).  Its own issue stream, so a wait here never
+// holds back the next SS MMAs.
+template <int D, bool kDQ>
+__device__ void b_ts(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy, uint32_t tmem,
+                     volatile int *abort) {
+  using C = BCfg<D, kDQ>;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
+  const long units = (long)P.B * P.h * npairs;
+  const uint64_t tm_desc = smem_desc_sw128(smem_u32(smem + C::kOffStage), 64 * 128, 1024);
+  uint32_t g = 0, ge = 0, ku = 0;
+  bool ok = true;
+  int k = 0;
+  for (long u = blockIdx.x; u < units && ok && !*abort; u += gridDim.x, ++k) {
+    const int ub = k & 1;
+    if (!mbar_wait(&sy->info_full[ub], (k >> 1) & 1, abort, P.status, kDevTimeout)) break;
+    const int n = info[ub].n;
+    if (n > 0) {
+      for (int e = 0; e < n; ++e, ++g, ++ge) {
+        const uint32_t st = ge % C::kStages;
+        const uint32_t b = g & 1u;
+        ok = mbar_wait(&sy->p_full[b], (g >> 1) & 1u, abort, P.status, kDevTimeout);
+        if (ok && e == 0 && ku > 0)
+          ok = mbar_wait(&sy->acc_free, (ku - 1) & 1u, abort, P.status, kDevTimeout);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t t1 = tm_desc + (uint64_t)((st * C::kStageBytes) >> 4);
+        const uint64_t t2 = tm_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
+          const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
+          const uint32_t acc = (e > 0 || kk > 0) ? 1u : 0u;
+          if (kDQ) {
+            mma_ts(tmem + C::kAcc1, tmem + C::kPD + b * 64 + kk * 8, t1 + dk, C::kIdTS, acc);
+          } else {  // entries 32 g .. 32 g + 31 sit at columns 32 g .. 32 g + 15 of X and Y
+            const uint32_t xb = tmem + C::kXY + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+            mma_ts(tmem + C::kAcc0, xb, t2 + dk, C::kIdTS, acc);       // dV += P^T dout
+            mma_ts(tmem + C::kAcc1, xb + 64, t1 + dk, C::kIdTS, acc);  // dK += dz^T q
+          }
+        }
+        // the stage (read by both streams; SS(g) finished before the softmax of
+        // step g began) and the P / dz of buffer b are free once these are done
+        mma_commit(&sy->st_empty[st]);
+        mma_commit(&sy->buf_free[b]);
+      }
+      if (!ok) break;
+      mma_commit(&sy->acc_full);
+      ++ku;
+    }
+    mbar_arrive(&sy->info_empty[ub]);
+  }
+  mma_commit(&sy->drain);
   mbar_wait(&sy->drain, 0, nullptr, P.status, kDevTimeout);
 }
 
@@ -478,7 +503,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sy->a_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sy->info_full[i], 1);
-      mbar_init(&sy->info_empty[i], C::kSoftmax + 1);  // softmax threads + the MMA issuer
+      mbar_init(&sy->info_empty[i], C::kSoftmax + 2);  // softmax threads + both MMA issuers
       mbar_init(&sy->p_full[i], C::kSoftmax);
       mbar_init(&sy->buf_free[i], 1);
       mbar_init(&sy->s_full[i], 1);
@@ -486,7 +511,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&sy->acc_full, 1);
     mbar_init(&sy->acc_free, C::kSoftmax);
-    mbar_init(&sy->drain, 1);
+    mbar_init(&sy->drain, 2);  // one commit per MMA-issuing thread
     sy->abort = 0;
     tma_prefetch_desc(&mA1);
     tma_prefetch_desc(&mA2);
@@ -507,7 +532,10 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0) {
     b_producer<D, kDQ>(Pp, &mA1, &mA2, &mT1, &mT2, smem, info, sy, abort);
   } else if (warp == 1) {
-    if (lane == 0) b_mma<D, kDQ>(Pp, smem, info, sy, tmem, abort);
+    if (lane == 0) b_ss<D, kDQ>(Pp, smem, info, sy, tmem, abort);
+    __syncwarp();
+  } else if (warp == 2) {
+    if (lane == 0) b_ts<D, kDQ>(Pp, smem, info, sy, tmem, abort);
     __syncwarp();
   } else if (warp >= 4) {
     b_softmax<D, kDQ>(Pp, smem, info, sy, tmem, abort);
