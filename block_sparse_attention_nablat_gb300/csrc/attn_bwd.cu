@@ -425,17 +425,9 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const void
                          const void *dout, const Shape &s, BwdArgs A, bool have_lse, void *dq,
                          void *dk, void *dv, cudaStream_t st) {
   auto prep = have_lse ? bwd_prep_kernel<T, D, false> : bwd_prep_kernel<T, D, true>;
-  auto dkdv = bwd_dkdv_kernel<T, D>;
-  auto dqk = bwd_dq_kernel<T, D>;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)prep_smem<D>())) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)dkdv_smem<D>())) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)dq_smem<D>())) != cudaSuccess)
     return e;
   const T *tq = static_cast<const T *>(q), *tk = static_cast<const T *>(k),
           *tv = static_cast<const T *>(v), *to = static_cast<const T *>(o),
@@ -455,14 +447,24 @@ cudaError_t launch_typed(const void *q, const void *k, const void *v, const void
   if ((e = launch_pdl(bwd_gather_kernel, dim3(warps_grid), dim3(kThreads), 0, st, A, rows)) !=
       cudaSuccess)
     return e;
-  if (std::is_same<T, __nv_bfloat16>::value)  // bf16: the products on the tensor cores
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {  // the products on the tensor cores
     return launch_attn_bwd_tc(q, k, v, dout, s, A.kv_nb, A.kv_inds, A.qt_nb, A.qt_inds, A.lse2,
                               A.delta, A.scale, dq, dk, dv, A.status, st);
-  if ((e = launch_pdl(dkdv, grid, dim3(kThreads), dkdv_smem<D>(), st, tq, tk, tv, tdo,
-                      static_cast<T *>(dk), static_cast<T *>(dv), A)) != cudaSuccess)
-    return e;
-  return launch_pdl(dqk, grid, dim3(kThreads), dq_smem<D>(), st, tq, tk, tv, tdo,
-                    static_cast<T *>(dq), A);
+  } else {  // fp32: the products on CUDA cores
+    auto dkdv = bwd_dkdv_kernel<T, D>;
+    auto dqk = bwd_dq_kernel<T, D>;
+    if ((e = cudaFuncSetAttribute(dkdv, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)dkdv_smem<D>())) != cudaSuccess)
+      return e;
+    if ((e = cudaFuncSetAttribute(dqk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)dq_smem<D>())) != cudaSuccess)
+      return e;
+    if ((e = launch_pdl(dkdv, grid, dim3(kThreads), dkdv_smem<D>(), st, tq, tk, tv, tdo,
+                        static_cast<T *>(dk), static_cast<T *>(dv), A)) != cudaSuccess)
+      return e;
+    return launch_pdl(dqk, grid, dim3(kThreads), dq_smem<D>(), st, tq, tk, tv, tdo,
+                      static_cast<T *>(dq), A);
+  }
 }
 
 }  // namespace

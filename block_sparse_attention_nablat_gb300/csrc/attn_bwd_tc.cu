@@ -476,7 +476,6 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
     }
     mbar_arrive(&sy->info_empty[ub]);  // done with this unit's bitmaps
   }
-  (void)lane;
 }
 
 template <int D, bool kDQ>
