@@ -7,10 +7,6 @@
 
 namespace nabla {
 
-cudaError_t launch_attn_tc(const void *q, const void *k, const void *v, const Shape &s,
-                           const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *o,
-                           float *lse, int *status, cudaStream_t st);
-
 namespace {
 
 constexpr int kMaxBlocks = 2048;

@@ -480,7 +480,8 @@ BwdWorkspace bwd_workspace_layout(const Shape &s) {
   w.qt_nb = w.delta + up(rows * 4);
   w.qt_inds = w.qt_nb + up(blocks * 4);
   w.bits = w.qt_inds + up(blocks * s.s1 * 4);
-  w.total = w.bits + up(blocks * w.words * 4);
+  w.o_scratch = w.bits + up(blocks * w.words * 4);
+  w.total = w.o_scratch + up((size_t)s.B * s.S * s.h * s.D * 2);
   return w;
 }
 
@@ -506,9 +507,16 @@ cudaError_t launch_attn_bwd(const void *q, const void *k, const void *v, const v
             w.words,
             status};
   if (dt == NABLA_BF16) {
+    bool have_lse = lse != nullptr;
+    if (!have_lse) {  // the tcgen05 forward gives lse2 (its o goes to scratch)
+      const cudaError_t e = launch_attn_tc(q, k, v, s, kv_nb, kv_inds, scale, ws + w.o_scratch,
+                                           reinterpret_cast<float *>(ws + w.lse2), status, st);
+      if (e != cudaSuccess) return e;
+      have_lse = true;
+    }
     if (s.D == 64)
-      return launch_typed<__nv_bfloat16, 64>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
-    return launch_typed<__nv_bfloat16, 128>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
+      return launch_typed<__nv_bfloat16, 64>(q, k, v, o, dout, s, A, have_lse, dq, dk, dv, st);
+    return launch_typed<__nv_bfloat16, 128>(q, k, v, o, dout, s, A, have_lse, dq, dk, dv, st);
   }
   if (s.D == 64) return launch_typed<float, 64>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);
   return launch_typed<float, 128>(q, k, v, o, dout, s, A, lse != nullptr, dq, dk, dv, st);

@@ -65,8 +65,10 @@ cudaError_t launch_sta(int T, int H, int W, int wt, int wh, int ww, uint8_t *sta
 // K7: block-sparse attention backward.  Workspace regions (bytes, 256-aligned):
 // lse2 and delta [B, h, S] fp32, the transposed CSR qt_nb [B, h, s1] and
 // qt_inds [B, h, s1, s1] int32, and the word rows [B, h, s1, words] uint32.
+// A bf16 o-sized scratch follows: with no caller lse, the bf16 path runs the
+// tcgen05 forward once to get lse2 (its o goes there).
 struct BwdWorkspace {
-  size_t lse2, delta, qt_nb, qt_inds, bits, total;
+  size_t lse2, delta, qt_nb, qt_inds, bits, o_scratch, total;
   int words;
 };
 BwdWorkspace bwd_workspace_layout(const Shape &s);
@@ -81,6 +83,10 @@ cudaError_t launch_attn_bwd_tc(const void *q, const void *k, const void *v, cons
                                const int32_t *qt_nb, const int32_t *qt_inds, const float *lse2,
                                const float *delta, float scale, void *dq, void *dk, void *dv,
                                int *status, cudaStream_t st);
+// K3: bf16 block-sparse attention on tcgen05 (lse optional).
+cudaError_t launch_attn_tc(const void *q, const void *k, const void *v, const Shape &s,
+                           const int32_t *kv_nb, const int32_t *kv_inds, float scale, void *o,
+                           float *lse, int *status, cudaStream_t st);
 // K3f: CUDA-core block-sparse attention (fp32 storage).
 cudaError_t launch_attn_simt(const void *q, const void *k, const void *v, nabla_dtype dt,
                              const Shape &s, const int32_t *kv_nb, const int32_t *kv_inds,

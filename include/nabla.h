@@ -239,16 +239,18 @@ nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nab
  *   q, k, v, o, dout  [B, S, h, D] device, element type dt.
  *   lse               [B, h, S] device fp32 (16-byte aligned) from
  *                     nabla_attn_fwd_lse for the same inputs, or NULL: the
- *                     library then computes it (one more pass over the kept
- *                     blocks, on CUDA cores).
+ *                     library then computes it (bf16: one tcgen05 forward;
+ *                     fp32: a pass over the kept blocks on CUDA cores).
  *   kv_nb, kv_inds    the mask, as for nabla_attn_fwd (bad entries are skipped
  *                     and reported as NABLA_ERR_BAD_INDEX).
  *   scale             the forward's softmax scale.
  *   dq, dk, dv        [B, S, h, D] device, element type dt, overwritten.
  *   workspace         device scratch of ws_bytes >= nabla_attn_bwd_workspace_bytes()
- *                     (256-byte aligned): the rows' log-sum-exp and delta, and
- *                     the transposed mask (for each key block, the query
- *                     blocks that kept it).
+ *                     (256-byte aligned): the rows' log-sum-exp and delta, the
+ *                     transposed mask (for each key block, the query blocks
+ *                     that kept it), and a bf16 o-sized scratch used when dt is
+ *                     bf16 and lse is NULL (the library then runs the tcgen05
+ *                     forward once to obtain lse).
  * Errors: NABLA_ERR_INVALID_ARG as for nabla_attn_fwd, for NULL or unaligned
  * o, dout, dq, dk, dv or workspace, an lse not 16-byte aligned, and a short
  * workspace.

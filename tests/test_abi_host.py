@@ -168,7 +168,7 @@ def test_attn_bwd_workspace_bytes(lib, shape):
         return (x + 255) // 256 * 256
 
     want = 2 * up(B * h * S * 4) + up(B * h * s1 * 4) + up(B * h * s1 * s1 * 4) + \
-        up(B * h * s1 * ((s1 + 31) // 32) * 4)
+        up(B * h * s1 * ((s1 + 31) // 32) * 4) + up(B * S * h * D * 2)
     assert lib.nabla_attn_bwd_workspace_bytes(*shape) == want
     assert lib.nabla_attn_bwd_workspace_bytes(1, 1000, 2, 64) == 0
 
