@@ -58,7 +58,9 @@ def test_raster_layer_through_fractal_order(nabla):
     ref = O.build_mask(of["q"], of["k"], O.sta_mask(*w.grid, 1, 1, 1), 0.8)
     nbh, indh = nb.cpu().numpy(), inds.cpu().numpy()
     got = _mask_of(nbh, indh, w.s1)
-    amb = O.ambiguous_blocks(ref["c"], ref["t"], O.sta_mask(*w.grid, 1, 1, 1))
+    sta_h = O.sta_mask(*w.grid, 1, 1, 1)
+    amb = O.ambiguous_blocks(ref["c"], ref["t"], sta_h) | O.near_tie_blocks(
+        ref["p"], ref["cdf_mask"], sta_h, 1e-5)
     assert np.array_equal(got[~amb], ref["mask"][~amb])
     oref = O.block_sparse_attention(of["q"], of["k"], of["v"], nbh, indh, w.scale)
     want = O.fractal_unflatten(oref, T, H, Wd, 8)
