@@ -134,6 +134,16 @@ __device__ __forceinline__ void pair_sync(int q4) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + q4) : "memory");
 }
 
+// A softmax warp's arrival on p_full / o_free / info_empty: each lane has
+// fenced its TMEM and shared-memory work before the warp sync, then lane 0
+// arrives for the warp -- eight arrivals per event instead of 256 atomics on
+// one barrier word, which sit on the PV issuer's critical path every step.
+constexpr int kSmArrivals = 8;
+__device__ __forceinline__ void sm_arrive(uint64_t *bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 // P for 32 scores: 2^(s * scale_log2 - m) in fp32 (row-sum accumulators updated),
 // packed to bf16 pairs and stored over 16 TMEM columns at taddr.
 __device__ __forceinline__ void exp_pack_store(const uint32_t (&r)[32], uint64_t sc2, uint64_t nm2,
@@ -570,7 +580,7 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
         tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(&bar.p_full[b]);
+      sm_arrive(&bar.p_full[b], lane);
     }
     // ---- epilogue: O / (l_0 + l_1) -> bf16; each group writes its half of the columns
     if (steps > 0) {
@@ -618,8 +628,8 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
       }
     }
     tc_fence_before();
-    if (steps > 0) mbar_arrive(bar.o_free);
-    mbar_arrive(&bar.info_empty[ub]);
+    if (steps > 0) sm_arrive(bar.o_free, lane);
+    sm_arrive(&bar.info_empty[ub], lane);
     gs += steps;
     if (!live) break;  // both halves of every pair leave at the same unit
   }
@@ -667,14 +677,14 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar.info_full[i], 1);
-      mbar_init(&bar.info_empty[i], 256 + 3);  // softmax threads, both MMA issuers, V loader
+      mbar_init(&bar.info_empty[i], kSmArrivals + 3);  // softmax warps, both MMA issuers, V loader
     }
     for (int i = 0; i < C::kSBufs; ++i) {
       mbar_init(&bar.s_full[i], 1);
-      mbar_init(&bar.p_full[i], 256);
+      mbar_init(&bar.p_full[i], kSmArrivals);
       mbar_init(&bar.pv_done[i], 1);
     }
-    mbar_init(bar.o_free, 256);
+    mbar_init(bar.o_free, kSmArrivals);
     mbar_init(bar.drain, 2);  // one commit per MMA-issuing thread
     *abort = 0;
     tma_prefetch_desc(&tmQ);
