@@ -40,7 +40,7 @@ METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM G
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the workload with the current kernels; the capture, its command and the
 # per-kernel split are in profiles/launches_720p_bf16.md.  Workloads not captured: null.
-NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 17.0895e9, "mask": 1.8261e9}}
+NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 18.5477e9, "mask": 1.8264e9}}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -432,6 +432,20 @@ def run_ours(args, w, thr):
 
         e2e_run(2)
         torch.cuda.synchronize()
+        # host-link rates on their own (outside the timed region): the e2e figure
+        # depends on them, and they differ between hosts
+        tc = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        tc[0].record(h2d_st)
+        upload(0, None)
+        tc[1].record(h2d_st)
+        tc[1].synchronize()
+        tc[2].record(d2h_st)
+        readback(0, tc[1])
+        tc[3].record(d2h_st)
+        tc[3].synchronize()
+        nbytes = q.numel() * q.element_size()
+        h2d_gbs = 3 * nbytes / (tc[0].elapsed_time(tc[1]) * 1e-3) / 1e9
+        d2h_gbs = nbytes / (tc[2].elapsed_time(tc[3]) * 1e-3) / 1e9
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         h2d_st.wait_event(e0)
@@ -443,11 +457,11 @@ def run_ours(args, w, thr):
                               device=dev)
         if dist is not None:
             dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-        nbytes = q.numel() * q.element_size()
         e2e = {"value": attn_flops(w, kept_all) / (e2e_ms.item() * 1e-3) / 1e12,
                "unit": "TFLOP/s", "ms_per_step": e2e_ms.item(),
                "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
-               "copies": "double-buffered on two copy streams, overlapping compute"}
+               "copies": "double-buffered on two copy streams, overlapping compute",
+               "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
         del bufs
 
     if rank != 0:
