@@ -447,12 +447,13 @@ def run_ours(args, w, thr):
         h2d_gbs = 3 * nbytes / (tc[0].elapsed_time(tc[1]) * 1e-3) / 1e9
         d2h_gbs = nbytes / (tc[2].elapsed_time(tc[3]) * 1e-3) / 1e9
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        h2d_st.wait_event(e0)
-        d2h_st.wait_event(e0)
-        e2e_run(args.steps)
-        e1.record(stream)
-        torch.cuda.synchronize()
+        with ClockSampler(gpu_id(dev)) as e2e_clocks:
+            e0.record(stream)
+            h2d_st.wait_event(e0)
+            d2h_st.wait_event(e0)
+            e2e_run(args.steps)
+            e1.record(stream)
+            torch.cuda.synchronize()
         e2e_ms = torch.tensor([e0.elapsed_time(e1) / args.steps], dtype=torch.float64,
                               device=dev)
         if dist is not None:
@@ -461,7 +462,7 @@ def run_ours(args, w, thr):
                "unit": "TFLOP/s", "ms_per_step": e2e_ms.item(),
                "h2d_bytes_per_step": 3 * nbytes, "d2h_bytes_per_step": nbytes,
                "copies": "double-buffered on two copy streams, overlapping compute",
-               "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs}
+               "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "clocks": e2e_clocks.summary()}
         del bufs
 
     if rank != 0:

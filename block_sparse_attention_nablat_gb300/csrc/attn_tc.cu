@@ -29,7 +29,9 @@
 //    buffers.  With three buffers, QK^T of step s+2 only has to wait for the PV
 //    of step s-1, which is already queued ahead of PV(s), so the tensor pipe
 //    never drains between steps.
-//  * Warp roles: warp 0 builds the unit's entry bitmaps from kv_inds and issues
+//  * Warp roles: warp 0 builds the unit's entry bitmaps from kv_inds, lists each
+//    entry's two membership bits in entry order (so the softmax threads read one
+//    16-bit pair per step instead of each scanning the bitmaps) and issues
 //    the TMA loads of Q (once per unit) and of the K pair slots, warp 3 those of
 //    the per-entry V tiles (two producers, so a wait for a V slot never holds
 //    back the next K pair); one thread of warp 1 issues every QK^T and one
@@ -65,6 +67,8 @@ using namespace tc;
 using namespace tcattn;
 
 
+constexpr int kMaxEntries = 32 * kMaxWords;  // entries of a unit (s1 <= 2048)
+
 template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;          // 64-column (128-byte) swizzle boxes
@@ -88,7 +92,8 @@ struct Cfg {
   static constexpr int kOffInfo = kOffV + kVStages * kTileBytes;
   static constexpr int kOffXmax = kOffInfo + 2 * (int)sizeof(UnitInfo);  // [2 parity][2 grp][128]
   static constexpr int kOffXl = kOffXmax + 2 * 2 * 128 * 4;             // [2 grp][128]
-  static constexpr int kOffBars = kOffXl + 2 * 128 * 4;
+  static constexpr int kOffFlags = kOffXl + 2 * 128 * 4;                // [2 unit buffers][kMaxEntries]
+  static constexpr int kOffBars = kOffFlags + 2 * kMaxEntries;
 };
 
 // All mbarriers and small shared flags, laid out by the compiler (8-byte aligned).
@@ -191,7 +196,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
                          volatile int *abort) {
   using C = Cfg<D>;
   const int lane = threadIdx.x & 31;
-  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1, words = (s1 + 31) >> 5;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   uint32_t gk = 0, ge = 0, kq = 0;  // K pair slots issued, (V: none here), Q tiles issued
   bool stop = false;  // lane 0: a wait gave up; every lane leaves together at the loop top
@@ -238,10 +243,33 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     }
     if (bad) atomicCAS(P.status, kDevOk, kDevBadIndex);
     __syncwarp();
-    int cnt = 0;
-    for (int w = lane; w < words; w += 32) cnt += __popc(inf.a[w] | inf.b[w]);
+    // entry count, and each entry's membership bits in entry order (ascending
+    // key block) for the softmax warps: lane l lists the entries of words 2l and
+    // 2l + 1, starting where the lanes before it end
+    static_assert(kMaxWords == 64, "two bitmap words per lane");
+    const uint32_t u0 = inf.a[2 * lane] | inf.b[2 * lane];
+    const uint32_t u1 = inf.a[2 * lane + 1] | inf.b[2 * lane + 1];
+    const int mine = __popc(u0) + __popc(u1);
+    int incl = mine;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int cnt = __shfl_sync(0xffffffffu, incl, 31);
+    {
+      uint8_t *fl = smem + C::kOffFlags + ub * kMaxEntries;
+      int pos = incl - mine;
+#pragma unroll
+      for (int hw = 0; hw < 2; ++hw) {
+        const int w = 2 * lane + hw;
+        const uint32_t aw = inf.a[w], bw = inf.b[w];
+        for (uint32_t m = hw ? u1 : u0; m; m &= m - 1u) {
+          const int bit = __ffs(m) - 1;
+          fl[pos++] = (uint8_t)(((aw >> bit) & 1u) | (((bw >> bit) & 1u) << 1));
+        }
+      }
+    }
     if (lane == 0) inf.n = cnt;
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.info_full[ub]);
@@ -478,13 +506,14 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
     const Unit un = decode(u, npairs, P.h);
     const int qb = pair_block(un.pr, half, P.pstride);
     float m_run = -INFINITY, l_run = 0.f;
-    Cursor cur{0, info[ub].a[0] | info[ub].b[0]};
+    // the two entries' membership bits of step s, one byte each, listed by the
+    // producer (one 16-bit load per step instead of a bitmap scan per thread)
+    const uint16_t *fl = reinterpret_cast<const uint16_t *>(smem + C::kOffFlags + ub * kMaxEntries);
     for (int s = 0; s < steps; ++s) {
       const uint32_t g = gs + s, b = g % C::kSBufs, use = g / C::kSBufs;
-      uint32_t f0 = 0, f1 = 0;
-      next_entry(info[ub], cur, f0);
       const bool has1 = 2 * s + 1 < n;
-      if (has1) next_entry(info[ub], cur, f1);
+      const uint32_t pr = fl[s];
+      const uint32_t f0 = pr & 0xffu, f1 = has1 ? pr >> 8 : 0u;
       const bool mine = grp == 0 || has1;
       const bool act = mine && ((((grp ? f1 : f0) >> half) & 1u) != 0u);
       live = __all_sync(0xffffffffu, live && mbar_wait(&bar.s_full[b], use & 1u, abort, P.status,
