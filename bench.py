@@ -40,7 +40,7 @@ METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM G
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the workload with the current kernels; the capture, its command and the
 # per-kernel split are in profiles/launches_720p_bf16.md.  Workloads not captured: null.
-NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 18.5477e9, "mask": 1.8264e9}}
+NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 20.4328e9, "mask": 1.8263e9}}
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
