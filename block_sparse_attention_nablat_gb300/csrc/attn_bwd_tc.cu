@@ -22,7 +22,9 @@
 // columns 32-63) load their X and Y columns and form
 //   dK/dV: P^T = 2^(X sl2 - lse2[col]),  dz^T = P^T (Y - delta[col]);
 //   dQ:    P   = 2^(X sl2 - lse2[row]),  dz   = P   (Y - delta[row]);
-// with P = 0 in the rows whose block did not keep the entry.  P and dz are
+// with P = 0 in the rows whose block did not keep the entry (the producer warp
+// lists each entry's membership bits once per unit, so the softmax threads
+// read one byte per entry instead of scanning the bitmaps).  P and dz are
 // stored as bf16 and TS MMAs accumulate
 //   dK/dV: dV += P^T dout, dK += dz^T q;   dQ: dQ += dz k.
 // One thread (warp 1) issues the SS MMAs and another (warp 2) the TS MMAs, so
@@ -66,7 +68,8 @@ struct BCfg {
   static constexpr int kOffA2 = kPairBytes;
   static constexpr int kOffStage = 2 * kPairBytes;
   static constexpr int kOffInfo = kOffStage + kStages * kStageBytes;
-  static constexpr int kOffBars = kOffInfo + 2 * (int)sizeof(UnitInfo);
+  static constexpr int kOffFlags = kOffInfo + 2 * (int)sizeof(UnitInfo);  // [2][kMaxEntries]
+  static constexpr int kOffBars = kOffFlags + 2 * kMaxEntries;
   static constexpr uint32_t kAcc1 = 0, kAcc0 = D;
   static constexpr uint32_t kXY = kDQ ? D : 2 * D;  // X / Y buffer b at kXY + 128 b
   static constexpr uint32_t kPD = D + 256;          // dQ: dz buffer b at kPD + 64 b
@@ -114,7 +117,7 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
                            UnitInfo *info, BSync *sy, volatile int *abort) {
   using C = BCfg<D, kDQ>;
   const int lane = threadIdx.x & 31;
-  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1, words = (s1 + 31) >> 5;
+  const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   uint32_t ge = 0, ka = 0;
   bool go = true;
@@ -158,10 +161,8 @@ __device__ void b_producer(const TcParams &P, const CUtensorMap *mA1, const CUte
     }
     if (bad) atomicCAS(P.status, kDevOk, kDevBadIndex);
     __syncwarp();
-    int cnt = 0;
-    for (int w = lane; w < words; w += 32) cnt += __popc(inf.a[w] | inf.b[w]);
-#pragma unroll
-    for (int o = 16; o; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    // entry count, and the entries' membership bits for the softmax warps
+    const int cnt = list_entries(inf, smem + C::kOffFlags + ub * kMaxEntries, lane);
     if (lane == 0) inf.n = cnt;
     __syncwarp();
     if (lane == 0) mbar_arrive(&sy->info_full[ub]);
@@ -389,11 +390,11 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
       lse_r = P.lse2[(size_t)bh * P.S + (size_t)blk * 64 + (row & 63)];
       dl_r = P.delta[(size_t)bh * P.S + (size_t)blk * 64 + (row & 63)];
     }
-    Cursor cur{0, info[ub].a[0] | info[ub].b[0]};
+    // each entry's membership bits, listed by the producer
+    const uint8_t *elist = smem + C::kOffFlags + ub * kMaxEntries;
     for (int e = 0; e < n && live; ++e, ++g, ++ge) {
       const uint32_t b = g & 1u, st = ge % C::kStages;
-      uint32_t fl;
-      next_entry(info[ub], cur, fl);
+      const uint32_t fl = elist[e];
       const bool act = ((fl >> side) & 1u) != 0u;
       live = __all_sync(0xffffffffu,
                         mbar_wait(&sy->s_full[b], (g >> 1) & 1u, abort, P.status, kDevTimeout));

@@ -28,6 +28,38 @@ struct Cursor {
   uint32_t m;
 };
 
+constexpr int kMaxEntries = 32 * kMaxWords;  // entries of a unit (s1 <= 2048)
+
+// Warp-wide: the unit's entry count, and each entry's two membership bits
+// (bit 0: first block of the pair, bit 1: second) written to fl[0 .. n) in
+// entry order (ascending key block).  Lane l lists the entries of bitmap words
+// 2l and 2l + 1, starting where the lanes before it end.  Lets the threads
+// that walk a unit's entries read one byte per entry instead of each
+// scanning the bitmaps.
+__device__ __forceinline__ int list_entries(const UnitInfo &inf, uint8_t *fl, int lane) {
+  static_assert(kMaxWords == 64, "two bitmap words per lane");
+  const uint32_t u0 = inf.a[2 * lane] | inf.b[2 * lane];
+  const uint32_t u1 = inf.a[2 * lane + 1] | inf.b[2 * lane + 1];
+  const int mine = __popc(u0) + __popc(u1);
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int pos = incl - mine;
+#pragma unroll
+  for (int hw = 0; hw < 2; ++hw) {
+    const int w = 2 * lane + hw;
+    const uint32_t aw = inf.a[w], bw = inf.b[w];
+    for (uint32_t m = hw ? u1 : u0; m; m &= m - 1u) {
+      const int bit = __ffs(m) - 1;
+      fl[pos++] = (uint8_t)(((aw >> bit) & 1u) | (((bw >> bit) & 1u) << 1));
+    }
+  }
+  return __shfl_sync(0xffffffffu, incl, 31);
+}
+
 __device__ __forceinline__ int next_entry(const UnitInfo &inf, Cursor &c, uint32_t &flags) {
   while (c.m == 0u && c.w + 1 < kMaxWords) {
     ++c.w;

@@ -67,8 +67,6 @@ using namespace tc;
 using namespace tcattn;
 
 
-constexpr int kMaxEntries = 32 * kMaxWords;  // entries of a unit (s1 <= 2048)
-
 template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;          // 64-column (128-byte) swizzle boxes
@@ -243,33 +241,8 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     }
     if (bad) atomicCAS(P.status, kDevOk, kDevBadIndex);
     __syncwarp();
-    // entry count, and each entry's membership bits in entry order (ascending
-    // key block) for the softmax warps: lane l lists the entries of words 2l and
-    // 2l + 1, starting where the lanes before it end
-    static_assert(kMaxWords == 64, "two bitmap words per lane");
-    const uint32_t u0 = inf.a[2 * lane] | inf.b[2 * lane];
-    const uint32_t u1 = inf.a[2 * lane + 1] | inf.b[2 * lane + 1];
-    const int mine = __popc(u0) + __popc(u1);
-    int incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int cnt = __shfl_sync(0xffffffffu, incl, 31);
-    {
-      uint8_t *fl = smem + C::kOffFlags + ub * kMaxEntries;
-      int pos = incl - mine;
-#pragma unroll
-      for (int hw = 0; hw < 2; ++hw) {
-        const int w = 2 * lane + hw;
-        const uint32_t aw = inf.a[w], bw = inf.b[w];
-        for (uint32_t m = hw ? u1 : u0; m; m &= m - 1u) {
-          const int bit = __ffs(m) - 1;
-          fl[pos++] = (uint8_t)(((aw >> bit) & 1u) | (((bw >> bit) & 1u) << 1));
-        }
-      }
-    }
+    // entry count, and the entries' membership bits for the softmax warps
+    const int cnt = list_entries(inf, smem + C::kOffFlags + ub * kMaxEntries, lane);
     if (lane == 0) inf.n = cnt;
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.info_full[ub]);
