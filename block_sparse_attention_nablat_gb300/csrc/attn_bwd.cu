@@ -9,7 +9,7 @@
 //   dz_su = P_su (dP_su - delta_s),  dq_s = scale sum_u dz_su k_u,
 //   dk_u = scale sum_s dz_su q_s.
 //
-// Four kernels:
+// Five kernels:
 //   prep     one CTA per query block: delta_s from the stored o, and the row's
 //            log-sum-exp over its kept list (base 2, scale folded in), so that
 //            P = 2^(z log2(e) - lse2) needs no second normalisation pass;
