@@ -234,7 +234,9 @@ nabla_status nabla_attn_fwd_lse(const void *q, const void *k, const void *v, nab
  * Rows with kv_nb = 0 contribute nothing (their dq is 0); key blocks that no
  * row kept get dk = dv = 0.  delta is formed from the o passed in, which
  * must be the forward output for the same inputs (as stored by a training
- * step).  Arithmetic is fp32 on CUDA cores; dq, dk, dv are written in dt.
+ * step).  fp32 storage: fp32 arithmetic on CUDA cores.  bf16 storage: the
+ * products run on tcgen05 with fp32 accumulation; P and dz enter the products
+ * as bf16, as the forward's P does.  dq, dk, dv are written in dt.
  *
  *   q, k, v, o, dout  [B, S, h, D] device, element type dt.
  *   lse               [B, h, S] device fp32 (16-byte aligned) from
