@@ -18,8 +18,9 @@
  *   - Every pointer argument is DEVICE memory owned by the caller.  q, k, v, o
  *     must be 16-byte aligned, the workspace 256-byte aligned, kv_nb and kv_inds
  *     4-byte aligned; sta has no alignment rule.  The library allocates no device memory
- *     and keeps no state between calls other than a per-kernel device status
- *     word (see nabla_get_last_device_status).
+ *     and keeps no state between calls other than a device status word (see
+ *     nabla_get_last_device_status) and the statically reserved scratch array
+ *     of nabla_build_mask_noalloc.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) of the CURRENT device.  A returned NABLA_OK means
  *     the arguments were valid and the kernels were launched.
