@@ -179,6 +179,26 @@ def test_sta_rejects(lib, args):
     assert lib.nabla_sta_mask(4, 2, 2, 1, 1, 1, None, None) == INVALID
 
 
+def _fractal(lib, flatten, **kw):
+    a = dict(src=FAKE, dt=1, B=1, T=2, H=16, W=16, h=2, D=64, P=8, dst=FAKE + (1 << 32), st=None)
+    a.update(kw)
+    fn = lib.nabla_fractal_flatten if flatten else lib.nabla_fractal_unflatten
+    return fn(a["src"], a["dt"], a["B"], a["T"], a["H"], a["W"], a["h"], a["D"], a["P"],
+              a["dst"], a["st"])
+
+
+@pytest.mark.parametrize("flatten", [True, False], ids=["flatten", "unflatten"])
+@pytest.mark.parametrize("kw", [dict(dt=7), dict(B=0), dict(T=0), dict(H=0), dict(P=0),
+                                dict(H=12), dict(W=20), dict(h=1, D=3), dict(src=None),
+                                dict(dst=None), dict(src=FAKE + 8), dict(dst=FAKE + (1 << 32) + 4),
+                                dict(dst=FAKE + 16)],
+                         ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_fractal_rejects(lib, flatten, kw):
+    """Ragged patches, rows that are not whole 16-byte chunks, NULL, unaligned and
+    overlapping buffers are refused on the host, before any launch."""
+    assert _fractal(lib, flatten, **kw) == INVALID
+
+
 def test_product_path_has_no_oracle_dependency():
     """The package and its native sources never import or link the oracle."""
     pkg = os.path.join(ROOT, "block_sparse_attention_nablat_gb300")
