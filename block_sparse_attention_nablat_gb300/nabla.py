@@ -111,6 +111,37 @@ def _shape(q: torch.Tensor) -> Tuple[int, int, int, int]:
     return tuple(q.shape)
 
 
+# The C ABI receives bare pointers and cannot see a buffer's size, element type
+# or device, so every tensor handed to it is checked here first: a short or
+# mistyped buffer, or one in host memory, would otherwise be read or written
+# out of bounds by the kernels.
+def _on(t: torch.Tensor, name: str, device: torch.device) -> None:
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _buf(t: torch.Tensor, name: str, numel: int, dtype: torch.dtype,
+         device: torch.device) -> None:
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.numel() < numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs {numel}")
+    _on(t, name, device)
+
+
+def _cuda(t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"tensors must be on a CUDA device, got {t.device}")
+
+
+def _csr(kv_nb: torch.Tensor, kv_inds: torch.Tensor, B: int, h: int, s1: int,
+         device: torch.device) -> None:
+    _buf(kv_nb, "kv_nb", B * h * s1, torch.int32, device)
+    _buf(kv_inds, "kv_inds", B * h * s1 * s1, torch.int32, device)
+
+
 def nabla_abi_version() -> int:
     return load().nabla_abi_version()
 
@@ -138,9 +169,14 @@ def nabla_build_mask(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor, thr: f
         kv_nb = torch.empty((B, h, s1), dtype=torch.int32, device=dev)
     if kv_inds is None:
         kv_inds = torch.empty((B, h, s1, s1), dtype=torch.int32, device=dev)
+    _on(k, "k", dev)
+    _buf(sta, "sta", s1 * s1, torch.uint8, dev)
+    _csr(kv_nb, kv_inds, B, h, s1, dev)
     need = lib.nabla_build_mask_workspace_bytes(B, S, h, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _on(workspace, "workspace", dev)
+    _cuda(q)
     st = lib.nabla_build_mask(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
                               float(thr), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _stream(stream))
@@ -153,6 +189,13 @@ def nabla_build_mask_noalloc(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor
     """nabla_build_mask without a workspace: the library's fixed device scratch is
     used instead (see include/nabla.h); outputs must be preallocated by the caller."""
     B, S, h, D = _shape(q)
+    if k.shape != q.shape or k.dtype != q.dtype:
+        raise ValueError("k must match q")
+    s1 = S // 64
+    _on(k, "k", q.device)
+    _buf(sta, "sta", s1 * s1, torch.uint8, q.device)
+    _csr(kv_nb, kv_inds, B, h, s1, q.device)
+    _cuda(q)
     st = load().nabla_build_mask_noalloc(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
                                          float(thr), _ptr(kv_nb), _ptr(kv_inds), _stream(stream))
     _check(st, "nabla_build_mask_noalloc")
@@ -175,9 +218,13 @@ def nabla_build_mask_topk(q: torch.Tensor, k: torch.Tensor, topk_ratio: float,
         kv_nb = torch.empty((B, h, s1), dtype=torch.int32, device=dev)
     if kv_inds is None:
         kv_inds = torch.empty((B, h, s1, s1), dtype=torch.int32, device=dev)
+    _on(k, "k", dev)
+    _csr(kv_nb, kv_inds, B, h, s1, dev)
     need = lib.nabla_build_mask_workspace_bytes(B, S, h, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _on(workspace, "workspace", dev)
+    _cuda(q)
     st = lib.nabla_build_mask_topk(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D,
                                    float(topk_ratio), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), _stream(stream))
@@ -197,6 +244,11 @@ def nabla_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb: tor
         scale = 1.0 / math.sqrt(D)
     if o is None:
         o = torch.empty_like(q)
+    _on(k, "k", q.device)
+    _on(v, "v", q.device)
+    _csr(kv_nb, kv_inds, B, h, S // 64, q.device)
+    _buf(o, "o", q.numel(), q.dtype, q.device)
+    _cuda(q)
     st = lib.nabla_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D, _ptr(kv_nb),
                             _ptr(kv_inds), float(scale), _ptr(o), _stream(stream))
     _check(st, "nabla_attn_fwd")
@@ -220,6 +272,12 @@ def nabla_attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb:
         scale = 1.0 / math.sqrt(D)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, h, S), dtype=torch.float32, device=q.device) if lse is None else lse
+    _on(k, "k", q.device)
+    _on(v, "v", q.device)
+    _csr(kv_nb, kv_inds, B, h, S // 64, q.device)
+    _buf(o, "o", q.numel(), q.dtype, q.device)
+    _buf(lse, "lse", B * h * S, torch.float32, q.device)
+    _cuda(q)
     st = lib.nabla_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D,
                                 _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(o), _ptr(lse),
                                 _stream(stream))
@@ -245,9 +303,18 @@ def nabla_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _on(t, name, q.device)
+    _csr(kv_nb, kv_inds, B, h, S // 64, q.device)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _buf(t, name, q.numel(), q.dtype, q.device)
+    if lse is not None:
+        _buf(lse, "lse", B * h * S, torch.float32, q.device)
     need = lib.nabla_attn_bwd_workspace_bytes(B, S, h, D)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _on(workspace, "workspace", q.device)
+    _cuda(q)
     st = lib.nabla_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                             _dtype_code(q), B, S, h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(dq), _ptr(dk),
                             _ptr(dv), _ptr(workspace),
@@ -263,6 +330,8 @@ def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=Non
     s1 = T * H * W
     if out is None:
         out = torch.empty((s1, s1), dtype=torch.uint8, device=device or "cuda")
+    _buf(out, "out", s1 * s1, torch.uint8, out.device)
+    _cuda(out)
     _check(lib.nabla_sta_mask(T, H, W, wt, wh, ww, _ptr(out), _stream(stream)),
            "nabla_sta_mask")
     return out
@@ -276,6 +345,8 @@ def nabla_fractal_flatten(x: torch.Tensor, P: int = 8, out: Optional[torch.Tenso
     B, T, H, W, h, D = x.shape
     if out is None:
         out = torch.empty((B, T * H * W, h, D), dtype=x.dtype, device=x.device)
+    _buf(out, "out", x.numel(), x.dtype, x.device)
+    _cuda(x)
     st = load().nabla_fractal_flatten(_ptr(x), _dtype_code(x), B, T, H, W, h, D, P, _ptr(out),
                                       _stream(stream))
     _check(st, "nabla_fractal_flatten")
@@ -290,6 +361,8 @@ def nabla_fractal_unflatten(y: torch.Tensor, T: int, H: int, W: int, P: int = 8,
     B, _, h, D = y.shape
     if out is None:
         out = torch.empty((B, T, H, W, h, D), dtype=y.dtype, device=y.device)
+    _buf(out, "out", y.numel(), y.dtype, y.device)
+    _cuda(y)
     st = load().nabla_fractal_unflatten(_ptr(y), _dtype_code(y), B, T, H, W, h, D, P, _ptr(out),
                                         _stream(stream))
     _check(st, "nabla_fractal_unflatten")
