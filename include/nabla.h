@@ -77,6 +77,15 @@ const char *nabla_status_string(nabla_status s);
  * as tf32 hi/lo pairs (four fp32 [B, h, s1, D] arrays) and the fp32 pooled map
  * ([B, h, s1, s1]), each region 256-byte aligned.  Returns 0 for an invalid
  * shape.
+ *
+ * After a nabla_build_mask call the workspace holds, for inspection (M =
+ * B*h*s1*D*4 rounded up to a multiple of 256 bytes):
+ *   [0, M)         hi parts of the query means times log2(e)/sqrt(D),
+ *   [M, 2M)        their lo parts,
+ *   [2M, 3M)       hi parts of the key means,   [3M, 4M) their lo parts,
+ *   [4M, 4M + B*h*s1*s1*4)  the pooled map in base-2 units,
+ *                  L[b,h,i,j] = <qa_i, ka_j> log2(e) / sqrt(D), fp32.
+ * Any bytes after these are private to the library.
  */
 size_t nabla_build_mask_workspace_bytes(int B, int S, int h, int D);
 
@@ -131,8 +140,12 @@ nabla_status nabla_build_mask(const void *q, const void *k, nabla_dtype dt, int 
  *     NABLA_NOALLOC_SCRATCH_BYTES are rejected with NABLA_ERR_UNSUPPORTED
  *     before anything is launched;
  *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress with that device current); make that first call
- *     before any stream capture;
+ *     (cudaGetSymbolAddress with that device current) and keeps it for the
+ *     process; make that first call before any stream capture.  First calls
+ *     from several host threads are safe (the lookup is serialised).  A
+ *     cudaDeviceReset unloads the library's device code and makes the kept
+ *     address stale: do not call this entry point on that device again in
+ *     the same process after a reset;
  *   - all calls share the one array, which keeps the last call's contents;
  *     the kernels overwrite every scratch element they read, so nothing needs
  *     clearing, but calls whose kernels overlap on the GPU (different streams,

@@ -182,28 +182,13 @@ def build_mask(q: np.ndarray, k: np.ndarray, sta: np.ndarray, thr: float):
 def ambiguous_blocks(c: np.ndarray, t: float, sta: Optional[np.ndarray] = None,
                      tol: float = 1e-4) -> np.ndarray:
     """Blocks whose running sum lies within tol of the cut level and that the STA
-    does not force on: the only places a float32 device result may differ."""
+    does not force on: the window of the stated mask tolerance, where a float32
+    device result may differ.  sta ([s1] for one row, [s1, s1] for a map) broadcasts
+    over the leading axes of c."""
     amb = np.abs(c - t) < tol
     if sta is not None:
-        amb &= ~np.asarray(sta, dtype=bool)[None, None]
+        amb &= ~np.asarray(sta, dtype=bool)
     return amb
-
-
-def near_tie_blocks(p: np.ndarray, cdf_mask: np.ndarray, sta: Optional[np.ndarray] = None,
-                    rel: float = 1e-5) -> np.ndarray:
-    """Blocks in a near-tie that straddles the cut (reading of the tolerance):
-    a dropped block j and a kept block k of the same row whose probabilities
-    differ by at most rel * max(p_j, p_k).  Their ascending order cannot be
-    resolved in float32, and swapping them moves each running sum by a whole
-    block mass, so either decision is admissible for both.  STA blocks excluded."""
-    dropped = ~cdf_mask
-    big = np.where(dropped, p, -np.inf).max(axis=-1, keepdims=True)  # heaviest dropped
-    small = np.where(cdf_mask, p, np.inf).min(axis=-1, keepdims=True)  # lightest kept
-    near = big >= small * (1.0 - rel)
-    out = near & ((dropped & (p >= small * (1.0 - rel))) | (cdf_mask & (p * (1.0 - rel) <= big)))
-    if sta is not None:
-        out &= ~np.asarray(sta, dtype=bool)[None, None]
-    return out
 
 
 # ---------------------------------------------------------------------------
@@ -233,10 +218,10 @@ def block_sparse_attention(q, k, v, kv_nb, kv_inds, scale: float,
             out[b, rows, hh, :] = 0.0
             continue
         blocks = np.asarray(kv_inds[b, hh, i, :n], dtype=np.int64)
-        tok = (blocks[:, None] * BLOCK + np.arange(BLOCK)[None, :]).ravel()
+        # the kept blocks' tokens, block by block in list order (64 rows each)
         Q = q[b, rows, hh, :].astype(np.float64)
-        K = k[b, tok, hh, :].astype(np.float64)
-        V = v[b, tok, hh, :].astype(np.float64)
+        K = np.asarray(k[b, :, hh, :].reshape(s1, BLOCK, D)[blocks].reshape(-1, D), np.float64)
+        V = np.asarray(v[b, :, hh, :].reshape(s1, BLOCK, D)[blocks].reshape(-1, D), np.float64)
         a = scale * (Q @ K.T)
         a -= a.max(axis=1, keepdims=True)
         e = np.exp(a)

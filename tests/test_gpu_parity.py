@@ -1,11 +1,13 @@
 """CUDA path vs the fp64 oracle, through the C ABI (needs an sm_103 GPU).
 
 Tolerances (the pages state none; these are the bounds this repository holds its kernels to):
-  mask: kv_nb / kv_inds bit-exact except blocks whose oracle running sum lies
-        within 1e-4 of 1 - thr (and that the STA does not force), and blocks in
-        a near-tie straddling the cut (probabilities within a relative 1e-5, an
-        order float32 cannot resolve); mismatches must be such blocks, and at
-        most 0.1% of all B*h*s1*s1 entries.
+  mask: kv_nb / kv_inds bit-exact except (a) blocks whose oracle running sum lies within
+        1e-4 of 1 - thr and that the STA does not force, and (b) blocks of a near tie
+        straddling the cut whose probabilities differ by less than the summed error
+        margins of the device's float32 arithmetic (derived per block in
+        tests/mask_tolerance.py); mismatches must be such blocks, and at most 0.1% of
+        all B*h*s1*s1 entries.  Window and near-tie mismatches are counted apart, and
+        every near-tie mismatch is listed with its relative gap and margin.
   attention, given the same mask: max-abs 1e-5 (fp32), max-abs 1e-2 and
         mean-abs 1e-3 (bf16).
 """
@@ -16,13 +18,13 @@ import numpy as np
 import pytest
 import torch
 
+import mask_tolerance as T
 from block_sparse_attention_nablat_gb300 import workloads as W
 from oracle import nabla_oracle as O
 
 pytestmark = pytest.mark.gpu
 
 AMB_TOL = 1e-4
-TIE_REL = 1e-5
 MAX_MISMATCH_FRAC = 1e-3
 TOL = {"f32": (1e-5, None), "bf16": (1e-2, 1e-3)}
 
@@ -76,24 +78,26 @@ def check_mask(w, thr, data, nb, inds, sta):
     ref = O.build_mask(qf, kf, sta, thr)
     got = csr_to_mask(nb, inds, w.s1)
     assert np.array_equal(nb, got.sum(-1))
+    theta = T.block_margins(qf, kf, ref["p"])
     window = O.ambiguous_blocks(ref["c"], ref["t"], sta, AMB_TOL)
-    ties = O.near_tie_blocks(ref["p"], ref["cdf_mask"], sta, TIE_REL)
+    ties = T.near_tie_blocks(ref["p"], ref["cdf_mask"], theta, sta)
     amb = window | ties
     mism = got != ref["mask"]
     n_mis = int(mism.sum())
+    rows, summary = T.mismatch_report(got, ref, window, ties, theta)
+    for r in rows:
+        print("MISMATCH", w.name, thr, r)
     bad = mism & ~amb
-    if bad.any():
-        for idx in list(zip(*np.nonzero(bad)))[:8]:
-            row = idx[:-1]
-            print("mismatch", idx, "p", ref["p"][idx], "c", ref["c"][idx], "t", ref["t"],
-                  "row kept", int(ref["mask"][row].sum()), "got", int(got[row].sum()))
-    assert not bad.any(), f"{int(bad.sum())} mismatches outside the admissible set"
+    assert not bad.any(), f"{int(bad.sum())} mismatches outside the admissible set: {rows[:8]}"
     assert n_mis <= MAX_MISMATCH_FRAC * mism.size
     assert np.all(got[:, :, sta.astype(bool)]), "an STA block was dropped"
     return {"density": float(got.mean()), "window": int(window.sum()),
             "near_tie": int(ties.sum()), "mismatches": n_mis,
-            "mismatch_in_window": int((mism & window).sum()),
-            "mismatch_near_tie": int((mism & ties & ~window).sum()),
+            "mismatch_in_window": summary["in_window"],
+            "mismatch_near_tie": summary["near_tie_only"],
+            "strict_outside_window": summary["outside_window"],
+            "worst_gap_over_margin": summary["worst_gap_over_margin"],
+            "margin_median": float(np.median(theta)),
             "entries": int(mism.size), "ref": ref}
 
 
@@ -106,6 +110,35 @@ def gpu_mask(nabla, w, data, thr):
     return nb.cpu().numpy(), inds.cpu().numpy(), sta.cpu().numpy()
 
 
+def oracle_attention(qf, kf, vf, nb, inds, scale, qblocks=None, workers=4):
+    """The oracle's block-sparse attention for the listed (b, h, i) query blocks (all if
+    None), called head by head (views of that head's q, k and v), several heads at a
+    time.  Returns float64 [B, S, h, D], NaN outside the listed blocks."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    B, S, h, D = qf.shape
+    s1 = S // 64
+    if qblocks is None:
+        qblocks = [(b, hh, i) for b in range(B) for hh in range(h) for i in range(s1)]
+    groups = {}
+    for b, hh, i in qblocks:
+        groups.setdefault((b, hh), []).append(i)
+    out = np.full((B, S, h, D), np.nan)
+
+    def one(key):
+        b, hh = key
+        o = O.block_sparse_attention(qf[b:b + 1, :, hh:hh + 1], kf[b:b + 1, :, hh:hh + 1],
+                                     vf[b:b + 1, :, hh:hh + 1], nb[b:b + 1, hh:hh + 1],
+                                     inds[b:b + 1, hh:hh + 1], scale,
+                                     [(0, 0, i) for i in groups[key]])
+        for i in groups[key]:
+            out[b, i * 64:(i + 1) * 64, hh, :] = o[0, i * 64:(i + 1) * 64, 0, :]
+
+    with ThreadPoolExecutor(workers) as ex:
+        list(ex.map(one, sorted(groups)))
+    return out
+
+
 def check_attention(nabla, w, data, nb, inds, qblocks=None, seed=0):
     dev_in = [nabla.from_storage(data[n], DEV) for n in "qkv"]
     o = nabla.nabla_attn_fwd(*dev_in, torch.from_numpy(nb).to(DEV),
@@ -113,7 +146,7 @@ def check_attention(nabla, w, data, nb, inds, qblocks=None, seed=0):
     assert nabla.nabla_get_last_device_status() == 0
     o = o.float().cpu().numpy()
     qf, kf, vf = (W.as_float(data[n]) for n in "qkv")
-    ref = O.block_sparse_attention(qf, kf, vf, nb, inds, w.scale, qblocks)
+    ref = oracle_attention(qf, kf, vf, nb, inds, w.scale, qblocks)
     sel = ~np.isnan(ref)
     err = np.abs(o[sel] - ref[sel])
     amax, amean = TOL[w.dtype]
@@ -130,6 +163,38 @@ def sample_qblocks(w, n, seed=0):
         out.add((int(rng.integers(w.B)), int(rng.integers(w.h)), int(rng.integers(w.s1))))
     # always include first and last blocks of the first head
     out |= {(0, 0, 0), (w.B - 1, w.h - 1, w.s1 - 1)}
+    return sorted(out)
+
+
+SMS = 152  # persistent attention CTAs: one per SM
+
+
+def cover_qblocks(w, per_bh=64, seed=0):
+    """Query blocks that reach every path of the attention kernel's work split.
+
+    The kernel pairs blocks i and i + d inside each run of 2d blocks, with d = 1 or a d
+    with 2d dividing s1 that it picks itself (on these grids the temporal neighbour
+    d = H*W), and hands the (batch, head, pair) units round-robin to one persistent CTA
+    per SM.  So for every (b, h): the first and last blocks, and random blocks together
+    with their partners at d = 1, W and H*W, until at least per_bh blocks are chosen;
+    and for the last (b, h), every block of the last 152 units at either stride (each
+    CTA's last unit)."""
+    Tg, Hg, Wg = w.grid
+    strides = [d for d in (1, Wg, Hg * Wg) if 2 * d <= w.s1 and w.s1 % (2 * d) == 0]
+    rng = np.random.default_rng(seed)
+    out = set()
+    for b in range(w.B):
+        for hh in range(w.h):
+            sel = {i for i in (0, 1, w.s1 - 2, w.s1 - 1) if 0 <= i < w.s1}
+            while len(sel) < min(per_bh, w.s1):
+                i = int(rng.integers(w.s1))
+                sel.add(i)
+                for d in strides:
+                    sel.add(i + d if i % (2 * d) < d else i - d)
+            out |= {(b, hh, i) for i in sel}
+    hw = Hg * Wg
+    tail = min(w.s1, 2 * hw * -(-SMS // hw), 2 * SMS + 2 * hw)
+    out |= {(w.B - 1, w.h - 1, i) for i in range(w.s1 - tail, w.s1)}
     return sorted(out)
 
 
@@ -175,8 +240,57 @@ def test_large_config_parity(nabla, name):
         st = check_mask(w, thr, data, nb, inds, sta)
         if thr == 1.0:
             assert np.all(nb == w.s1)
-        err = check_attention(nabla, w, data, nb, inds, sample_qblocks(w, 12, seed=n))
-        print("PARITY", name, thr, {k: v for k, v in st.items() if k != "ref"}, err)
+        qbs = cover_qblocks(w, 64, seed=n)
+        err = check_attention(nabla, w, data, nb, inds, qbs)
+        print("PARITY", name, thr, {k: v for k, v in st.items() if k != "ref"}, err,
+              f"attention checked on {len(qbs)} query blocks")
+
+
+@pytest.mark.slow
+def test_480p_attention_every_query_block(nabla):
+    """The whole 480p attention output (all 12,288 query blocks, ~8 TFLOP of fp64 on
+    the host) against the oracle, with the GPU's own mask."""
+    w = W.WORKLOADS["480p_bf16"]
+    data = inputs(w)
+    nb, inds, sta = gpu_mask(nabla, w, data, w.thr[0])
+    t0 = time.perf_counter()
+    err = check_attention(nabla, w, data, nb, inds)
+    print("FULL480", {"max_abs": err[0], "mean_abs": err[1],
+                      "kept_blocks": int(nb.sum()), "oracle_s": time.perf_counter() - t0})
+
+
+def _map_from_workspace(ws, w):
+    """The pooled map region of a mask-builder workspace (layout in include/nabla.h)."""
+    M = -(-(w.B * w.h * w.s1 * w.D * 4) // 256) * 256
+    n = w.B * w.h * w.s1 * w.s1
+    return ws[4 * M:4 * M + 4 * n].view(torch.float32).reshape(w.B, w.h, w.s1, w.s1)
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "small_bf16", "480p_bf16", "720p_bf16"])
+def test_pooled_map_within_derived_bound(nabla, name):
+    """Every entry of the device's pooled map (base-2 logits, read back from the
+    workspace) lies within the error bound derived from the kernels' arithmetic
+    (tests/mask_tolerance.py) of the exact fp64 logits: this pins the margins the
+    near-tie allowance of the mask tolerance rests on."""
+    w = W.WORKLOADS[name]
+    data = inputs(w)
+    q, k = (nabla.from_storage(data[n], DEV) for n in "qk")
+    sta = nabla.nabla_sta_mask(*w.grid, *w.sta_half_widths, device=DEV)
+    ws = torch.empty(nabla.nabla_build_mask_workspace_bytes(w.B, w.S, w.h, w.D),
+                     dtype=torch.uint8, device=DEV)
+    nabla.nabla_build_mask(q, k, sta, w.thr[0], workspace=ws)
+    assert nabla.nabla_get_last_device_status() == 0
+    Ld = _map_from_workspace(ws, w).cpu().numpy().astype(np.float64)
+    qf, kf = W.as_float(data["q"]), W.as_float(data["k"])
+    Lx = O.pooled_logits(O.pool_blocks(qf), O.pool_blocks(kf)) * math.log2(math.e)
+    U = T.logit_error_bound(qf, kf)
+    err = np.abs(Ld - Lx)
+    ratio = err / U
+    print("MAPERR", name, {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+                           "max_over_bound": float(ratio.max()),
+                           "p99_over_bound": float(np.quantile(ratio, 0.99)),
+                           "bound_median": float(np.median(U))})
+    assert np.all(err <= U), float(ratio.max())
 
 
 # ----------------------------------------------------------------------------- edge cases

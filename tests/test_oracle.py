@@ -125,13 +125,3 @@ def test_generator_deterministic_and_shaped():
     x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5], np.float32)
     assert np.array_equal(W.bf16_bits_to_f32(W.f32_to_bf16_bits(x)),
                           np.array([1.0, 1.0, 1.0 + 2 ** -6, -2.5], np.float32))
-
-
-def test_near_tie_blocks_closed_form():
-    """A dropped and a kept block whose probabilities differ by less than the
-    relative tolerance are both flagged; well-separated rows flag nothing."""
-    p = np.array([[0.1, 0.2, 0.3, 0.4], [0.1, 0.3, 0.3 * (1 + 2e-6), 0.3 - 2e-6 * 0.3 + 0.0]])
-    keep = np.array([[False, True, True, True], [False, False, True, True]])
-    got = O.near_tie_blocks(p, keep, rel=1e-5)
-    assert not got[0].any()
-    assert got[1, 1] and got[1, 2] and got[1, 3] and not got[1, 0]
