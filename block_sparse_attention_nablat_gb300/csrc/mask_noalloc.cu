@@ -3,6 +3,8 @@
 // array this file defines in device memory, so the caller passes only inputs
 // and outputs.  The array is created when the library's device code is loaded
 // and stays reserved on every GPU that loads it until the process exits.
+#include <mutex>
+
 #include "internal.h"
 
 namespace {
@@ -15,14 +17,19 @@ static_assert(kScratchBytes % 256 == 0, "scratch size must keep 256-byte alignme
 static __device__ __align__(256) unsigned char g_mask_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;            // guards the table below: first calls may race
 void *g_scratch_addr[kMaxDevices];  // device address of g_mask_scratch, per device
 
-// Set-up, once per device, with that device current.
+// Set-up, once per device, with that device current.  A cudaDeviceReset
+// unloads the library's device code, so an address taken before it is stale;
+// the header states that the entry point is then not to be used again on that
+// device in this process.
 cudaError_t scratch_address(void **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_addr[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_mask_scratch);

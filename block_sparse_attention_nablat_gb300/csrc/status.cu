@@ -20,27 +20,17 @@ __global__ void bounded_wait_probe(uint64_t limit_ns) {
     nabla::tc::mbar_wait(&bar, 0, nullptr, &g_status, nabla::kDevTimeout, limit_ns);
 }
 
-constexpr int kMaxDevices = 64;
-int *g_status_addr[kMaxDevices];
 }  // namespace
 
 namespace nabla {
 
+// Looked up on every call rather than cached: the lookup is a host-side table
+// query, it is safe from any host thread, and it stays right after a
+// cudaDeviceReset reloads the library's device code at another address.
 int *device_status_ptr(cudaError_t *err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxDevices) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  if (!g_status_addr[dev]) {
-    void *p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_status);
-    if (*err != cudaSuccess) return nullptr;
-    g_status_addr[dev] = static_cast<int *>(p);
-  }
-  return g_status_addr[dev];
+  void *p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_status);
+  return *err == cudaSuccess ? static_cast<int *>(p) : nullptr;
 }
 
 cudaError_t launch_bounded_wait_probe(cudaStream_t st) {

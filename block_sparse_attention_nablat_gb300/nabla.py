@@ -84,10 +84,19 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device: torch.device) -> Optional[int]:
+    """The cudaStream_t to launch on: the given one, else torch's current stream of
+    the tensors' device (not of whichever device happens to be current)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _call(device: torch.device, fn, *args) -> int:
+    """Run one C-ABI call with the tensors' device current: the library launches on,
+    and takes its per-device state from, the current device."""
+    with torch.cuda.device(device):
+        return fn(*args)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -177,9 +186,9 @@ def nabla_build_mask(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor, thr: f
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _on(workspace, "workspace", dev)
     _cuda(q)
-    st = lib.nabla_build_mask(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
-                              float(thr), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
-                              workspace.numel() * workspace.element_size(), _stream(stream))
+    st = _call(dev, lib.nabla_build_mask, _ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
+               float(thr), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
+               workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check(st, "nabla_build_mask")
     return kv_nb, kv_inds
 
@@ -196,8 +205,8 @@ def nabla_build_mask_noalloc(q: torch.Tensor, k: torch.Tensor, sta: torch.Tensor
     _buf(sta, "sta", s1 * s1, torch.uint8, q.device)
     _csr(kv_nb, kv_inds, B, h, s1, q.device)
     _cuda(q)
-    st = load().nabla_build_mask_noalloc(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D, _ptr(sta),
-                                         float(thr), _ptr(kv_nb), _ptr(kv_inds), _stream(stream))
+    st = _call(q.device, load().nabla_build_mask_noalloc, _ptr(q), _ptr(k), _dtype_code(q), B, S,
+               h, D, _ptr(sta), float(thr), _ptr(kv_nb), _ptr(kv_inds), _stream(stream, q.device))
     _check(st, "nabla_build_mask_noalloc")
     return kv_nb, kv_inds
 
@@ -225,9 +234,9 @@ def nabla_build_mask_topk(q: torch.Tensor, k: torch.Tensor, topk_ratio: float,
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     _on(workspace, "workspace", dev)
     _cuda(q)
-    st = lib.nabla_build_mask_topk(_ptr(q), _ptr(k), _dtype_code(q), B, S, h, D,
-                                   float(topk_ratio), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), _stream(stream))
+    st = _call(dev, lib.nabla_build_mask_topk, _ptr(q), _ptr(k), _dtype_code(q), B, S, h, D,
+               float(topk_ratio), _ptr(kv_nb), _ptr(kv_inds), _ptr(workspace),
+               workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check(st, "nabla_build_mask_topk")
     return kv_nb, kv_inds
 
@@ -249,8 +258,8 @@ def nabla_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb: tor
     _csr(kv_nb, kv_inds, B, h, S // 64, q.device)
     _buf(o, "o", q.numel(), q.dtype, q.device)
     _cuda(q)
-    st = lib.nabla_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D, _ptr(kv_nb),
-                            _ptr(kv_inds), float(scale), _ptr(o), _stream(stream))
+    st = _call(q.device, lib.nabla_attn_fwd, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D,
+               _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(o), _stream(stream, q.device))
     _check(st, "nabla_attn_fwd")
     return o
 
@@ -278,9 +287,9 @@ def nabla_attn_fwd_lse(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, kv_nb:
     _buf(o, "o", q.numel(), q.dtype, q.device)
     _buf(lse, "lse", B * h * S, torch.float32, q.device)
     _cuda(q)
-    st = lib.nabla_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S, h, D,
-                                _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(o), _ptr(lse),
-                                _stream(stream))
+    st = _call(q.device, lib.nabla_attn_fwd_lse, _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, S,
+               h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(o), _ptr(lse),
+               _stream(stream, q.device))
     _check(st, "nabla_attn_fwd_lse")
     return o, lse
 
@@ -315,10 +324,10 @@ def nabla_attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.T
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     _on(workspace, "workspace", q.device)
     _cuda(q)
-    st = lib.nabla_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
-                            _dtype_code(q), B, S, h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale), _ptr(dq), _ptr(dk),
-                            _ptr(dv), _ptr(workspace),
-                            workspace.numel() * workspace.element_size(), _stream(stream))
+    st = _call(q.device, lib.nabla_attn_bwd, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+               _ptr(dout), _dtype_code(q), B, S, h, D, _ptr(kv_nb), _ptr(kv_inds), float(scale),
+               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+               workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     _check(st, "nabla_attn_bwd")
     return dq, dk, dv
 
@@ -332,8 +341,9 @@ def nabla_sta_mask(T: int, H: int, W: int, wt: int, wh: int, ww: int, device=Non
         out = torch.empty((s1, s1), dtype=torch.uint8, device=device or "cuda")
     _buf(out, "out", s1 * s1, torch.uint8, out.device)
     _cuda(out)
-    _check(lib.nabla_sta_mask(T, H, W, wt, wh, ww, _ptr(out), _stream(stream)),
-           "nabla_sta_mask")
+    st = _call(out.device, lib.nabla_sta_mask, T, H, W, wt, wh, ww, _ptr(out),
+               _stream(stream, out.device))
+    _check(st, "nabla_sta_mask")
     return out
 
 
@@ -347,8 +357,8 @@ def nabla_fractal_flatten(x: torch.Tensor, P: int = 8, out: Optional[torch.Tenso
         out = torch.empty((B, T * H * W, h, D), dtype=x.dtype, device=x.device)
     _buf(out, "out", x.numel(), x.dtype, x.device)
     _cuda(x)
-    st = load().nabla_fractal_flatten(_ptr(x), _dtype_code(x), B, T, H, W, h, D, P, _ptr(out),
-                                      _stream(stream))
+    st = _call(x.device, load().nabla_fractal_flatten, _ptr(x), _dtype_code(x), B, T, H, W, h, D,
+               P, _ptr(out), _stream(stream, x.device))
     _check(st, "nabla_fractal_flatten")
     return out
 
@@ -363,20 +373,29 @@ def nabla_fractal_unflatten(y: torch.Tensor, T: int, H: int, W: int, P: int = 8,
         out = torch.empty((B, T, H, W, h, D), dtype=y.dtype, device=y.device)
     _buf(out, "out", y.numel(), y.dtype, y.device)
     _cuda(y)
-    st = load().nabla_fractal_unflatten(_ptr(y), _dtype_code(y), B, T, H, W, h, D, P, _ptr(out),
-                                        _stream(stream))
+    st = _call(y.device, load().nabla_fractal_unflatten, _ptr(y), _dtype_code(y), B, T, H, W, h, D,
+               P, _ptr(out), _stream(stream, y.device))
     _check(st, "nabla_fractal_unflatten")
     return out
 
 
+def _stream_device(stream) -> torch.device:
+    dev = getattr(stream, "device", None)
+    return torch.device(dev) if dev is not None else torch.device(
+        "cuda", torch.cuda.current_device())
+
+
 def nabla_selftest_bounded_wait(stream=None) -> None:
     """Enqueue the bounded-wait probe (it must end as a recorded timeout)."""
-    _check(load().nabla_selftest_bounded_wait(_stream(stream)), "nabla_selftest_bounded_wait")
+    dev = _stream_device(stream)
+    st = _call(dev, load().nabla_selftest_bounded_wait, _stream(stream, dev))
+    _check(st, "nabla_selftest_bounded_wait")
 
 
 def nabla_get_last_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
-    return load().nabla_get_last_device_status(_stream(stream))
+    dev = _stream_device(stream)
+    return _call(dev, load().nabla_get_last_device_status, _stream(stream, dev))
 
 
 def from_storage(a: np.ndarray, device) -> torch.Tensor:

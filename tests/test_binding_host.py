@@ -126,3 +126,32 @@ def test_fractal_and_sta_outputs_are_checked():
                                                   device="meta"))
     with pytest.raises(ValueError, match="out must be torch.uint8"):
         N.nabla_sta_mask(4, 2, 2, 1, 1, 1, out=torch.empty(16, 16, dtype=torch.int32))
+
+
+def test_calls_run_with_the_tensors_device_current(monkeypatch):
+    """The library launches on the current device and takes its per-device state
+    from it, so the binding makes the tensors' device current for each call and
+    takes the default stream from that device (not from whichever is current)."""
+    seen = []
+
+    class FakeDevice:
+        def __init__(self, d):
+            self.d = d
+
+        def __enter__(self):
+            seen.append(("enter", str(self.d)))
+
+        def __exit__(self, *exc):
+            seen.append(("exit", str(self.d)))
+
+    class FakeStream:
+        cuda_stream = 1234
+
+    monkeypatch.setattr(torch.cuda, "device", FakeDevice)
+    monkeypatch.setattr(torch.cuda, "current_stream",
+                        lambda d=None: seen.append(("stream", str(d))) or FakeStream())
+    dev = torch.device("cuda", 1)
+    got = N._call(dev, lambda *a: seen.append(("call", a)) or 0, N._stream(None, dev))
+    assert got == 0
+    assert seen == [("stream", "cuda:1"), ("enter", "cuda:1"), ("call", (1234,)),
+                    ("exit", "cuda:1")]

@@ -39,8 +39,9 @@ def test_noalloc_rejects_on_the_host():
     device work (so this runs without a GPU)."""
     _, lib = _lib()
     fake = 1 << 20
-    big = (1, 98304, 24, 128)  # 720p-like: ~264 MB of scratch
-    assert lib.nabla_build_mask_workspace_bytes(*big) > LIMIT
+    big = (1, 98304, 24, 128)  # 720p-like: four 18.9 MB mean arrays + a 226 MB map
+    need = lib.nabla_build_mask_workspace_bytes(*big)
+    assert need > LIMIT and abs(need - 301.7e6) < 1e6, need
     assert _call(lib, fake, fake, 1, big, fake, 0.9, fake, fake) == UNSUPPORTED
     assert _call(lib, fake, fake, 1, (1, 1000, 2, 64), fake, 0.9, fake, fake) == INVALID
     assert _call(lib, fake, fake, 1, (1, 1024, 2, 64), fake, 0.0, fake, fake) == INVALID
@@ -66,11 +67,20 @@ def test_noalloc_matches_workspace_entry_point_two_calls():
         ref_nb, ref_inds = nabla.nabla_build_mask(q, k, sta, thr)
         nb = torch.full((w.B, w.h, w.s1), -1, dtype=torch.int32, device=dev)
         inds = torch.full((w.B, w.h, w.s1, w.s1), -1, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        allocated = torch.cuda.memory_allocated(dev)
+        free = torch.cuda.mem_get_info(dev)[0]
         st = _call(lib, q.data_ptr(), k.data_ptr(), 1 if w.dtype == "bf16" else 0,
                    (w.B, w.S, w.h, w.D), sta.data_ptr(), thr, nb.data_ptr(), inds.data_ptr(),
                    torch.cuda.current_stream().cuda_stream)
         assert st == OK
         assert nabla.nabla_get_last_device_status() == 0
+        # nothing was allocated: torch's pool is untouched, and from the second call on
+        # (the first may be what loads the library's static array, with lazy module
+        # loading) the device's free memory is what it was before the call
+        assert torch.cuda.memory_allocated(dev) == allocated
+        if w is not cases[0][0]:
+            assert torch.cuda.mem_get_info(dev)[0] == free
         a_nb, b_nb = ref_nb.cpu().numpy(), nb.cpu().numpy()
         assert np.array_equal(a_nb, b_nb)
         a, b = ref_inds.cpu().numpy(), inds.cpu().numpy()
