@@ -38,10 +38,32 @@ from block_sparse_attention_nablat_gb300 import workloads as W  # noqa: E402
 
 METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM GB/s"
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the workload with the current kernels; the capture, its command and the
-# per-kernel split are in profiles/launches_720p_bf16.md.  Workloads not captured: null.
-NCU_TRAFFIC_BYTES = {"720p_bf16": {"attention": 20.4328e9, "mask": 1.8263e9}}
+# launch-list capture of the workload, with the kernel versions the capture saw; an
+# entry is dropped (reported as null) when its kernels change.  Workloads not
+# captured: null.
+NCU_TRAFFIC = {
+    "720p_bf16": {
+        "attention": {"bytes": 20.4328e9,
+                      "source": "ncu launch list, 720p, attn_tc_kernel with per-entry "
+                                "membership list and streaming o stores"},
+        "mask": {"bytes": 1.8263e9,
+                 "source": "ncu launch list, 720p, pool + pooled_map + select kernels"},
+    }
+}
+# the library kernels one step launches: pool, pooled map, select, attention
+KERNELS_PER_STEP = 4
+MASK_KERNELS = "mask build (pool + map + select)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def traffic_bytes(w, part):
+    e = NCU_TRAFFIC.get(w.name, {}).get(part)
+    return None if e is None else e["bytes"]
+
+
+def traffic_source(w, part):
+    e = NCU_TRAFFIC.get(w.name, {}).get(part)
+    return None if e is None else e["source"]
 
 
 def load_peaks():
@@ -293,6 +315,19 @@ def run_ours(args, w, thr):
     mask_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     assert nabla.nabla_get_last_device_status() == 0
+    # The same steps with nothing recorded between a step's mask build and its
+    # attention (one event pair around all K), as a user's loop runs them: the
+    # attention's launch and prologue then overlap the mask build's tail through
+    # the chained launches.  Timed after the region above, not part of `value`.
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    for s in range(args.steps):
+        step()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chained_ms = c0.elapsed_time(c1) / args.steps
+    assert nabla.nabla_get_last_device_status() == 0
 
     total_ms, kept_all = reduce_over_ranks(dist, dev, total_ms, kept)
     ms_per_step = total_ms / args.steps
@@ -475,6 +510,7 @@ def run_ours(args, w, thr):
     peaks, src = load_peaks()
     attn_tflops = attn_flops(w, kept) / (attn_ms * 1e-3) / 1e12
     peak_t = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    peak_b = peaks["bf16_tflops"]
     mask_gbs = mask_bytes(w, kept) / (mask_ms * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -499,25 +535,144 @@ def run_ours(args, w, thr):
                    "parallelism": f"replicas x{world}"},
         "parts": {"mask_build_us": mask_ms * 1e3, "mask_build_gbs": mask_gbs,
                   "attn_ms": attn_ms, "attn_tflops_kept": attn_tflops,
-                  "attn_tflops_dense_equiv": dense_flops(w) / (attn_ms * 1e-3) / 1e12},
+                  "attn_tflops_dense_equiv": dense_flops(w) / (attn_ms * 1e-3) / 1e12,
+                  "step_ms_chained": chained_ms,
+                  "chained_saving_us": (mask_ms + attn_ms - chained_ms) * 1e3},
         "roofline": {"bound": "tensor", "kernel": "attention forward", "achieved": attn_tflops,
                      "peak": peak_t, "unit": "TFLOP/s", "frac": attn_tflops / peak_t,
-                     "traffic": NCU_TRAFFIC_BYTES.get(w.name, {}).get("attention"),
-                     "peak_source": f"{src} bf16 sustained"},
-        "mask_roofline": {"bound": "hbm", "kernel": "mask build (pool + map + select)",
-                          "achieved": mask_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "peak_source": f"{src} bf16 sustained (the kernel runs inside a long step)",
+                     "peak_burst": peak_b, "frac_of_burst": attn_tflops / peak_b,
+                     "traffic": traffic_bytes(w, "attention"),
+                     "traffic_source": traffic_source(w, "attention")},
+        "mask_roofline": {"bound": "hbm", "kernel": MASK_KERNELS, "achieved": mask_gbs,
+                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                           "frac": mask_gbs / peaks["hbm_gbs"], "frac_of_8000": mask_gbs / 8000.0,
-                          "traffic": NCU_TRAFFIC_BYTES.get(w.name, {}).get("mask"),
+                          "traffic": traffic_bytes(w, "mask"),
+                          "traffic_source": traffic_source(w, "mask"),
                           "peak_source": f"{src} hbm"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "extras": extras,
-        "gpu_launches": args.steps * 4,
+        "gpu_launches": args.steps * KERNELS_PER_STEP,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+TABLE_ROWS = ([("tiny_f32", 0.9), ("small_bf16", 0.9), ("480p_bf16", 0.8), ("720p_bf16", 0.9)]
+              + [("sweep_bf16", t) for t in (0.5, 0.7, 0.9, 0.99, 1.0)])
+
+
+def table_cpu_leg(w, data, sta_h, thr, nb_h, inds_h, n_qblocks=8):
+    """The CPU-baseline leg of one table row: the oracle as it stands, on the host
+    cores -- the whole mask build (timed), its near-threshold blocks and how the GPU's
+    mask compares with it, and the attention for n_qblocks query blocks of the first
+    (batch, head), its time extrapolated to the whole workload by kept blocks."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import mask_tolerance as T
+    from oracle import nabla_oracle as O
+
+    qf, kf = W.as_float(data["q"]), W.as_float(data["k"])
+    t0 = time.perf_counter()
+    ref = O.build_mask(qf, kf, sta_h, thr)
+    t_mask = time.perf_counter() - t0
+    s1 = w.s1
+    pos = np.arange(s1)[None, None, None, :]
+    got = np.zeros(ref["mask"].shape, bool)
+    sel = np.where(pos < nb_h[..., None], inds_h, s1).astype(np.int64)
+    full = np.zeros(got.shape[:-1] + (s1 + 1,), bool)
+    np.put_along_axis(full, sel, True, axis=-1)
+    got = full[..., :s1]
+    theta = T.block_margins(qf, kf, ref["p"])
+    window = O.ambiguous_blocks(ref["c"], ref["t"], sta_h)
+    ties = T.near_tie_blocks(ref["p"], ref["cdf_mask"], theta, sta_h)
+    mism = got != ref["mask"]
+    rng = np.random.default_rng(0)
+    qb = sorted({int(x) for x in rng.integers(0, s1, n_qblocks)})
+    vf = W.as_float(data["v"])
+    t0 = time.perf_counter()
+    O.block_sparse_attention(qf[:1, :, :1], kf[:1, :, :1], vf[:1, :, :1], nb_h[:1, :1],
+                             inds_h[:1, :1], w.scale, [(0, 0, i) for i in qb])
+    t_att = time.perf_counter() - t0
+    kept_sample = int(sum(int(nb_h[0, 0, i]) for i in qb))
+    total_kept = int(nb_h.sum())
+    return {"kind": "oracle", "cores": host_cores(), "oracle_mask_s": t_mask,
+            "oracle_attn_s_extrapolated": t_att * total_kept / max(1, kept_sample),
+            "sample": f"mask: whole workload; attention: {len(qb)} query blocks of "
+                      f"(b, h) = (0, 0), time scaled by kept blocks",
+            "window_blocks": int(window.sum()), "near_tie_blocks": int(ties.sum()),
+            "mismatches": int(mism.sum()), "mismatch_in_window": int((mism & window).sum()),
+            "mismatch_near_tie_only": int((mism & ties & ~window).sum()),
+            "mismatch_outside_both": int((mism & ~window & ~ties).sum()),
+            "entries": int(mism.size)}
+
+
+def run_table(args):
+    """One JSON line per seeded configuration (and per threshold of the sweep): mask
+    build and attention, each timed on its own with CUDA events, plus the oracle leg."""
+    import torch
+    from block_sparse_attention_nablat_gb300 import nabla
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    nabla.load()
+    peaks, src = load_peaks()
+    stream = torch.cuda.current_stream()
+    cache = {}
+    rows = TABLE_ROWS if not args.table_only else [
+        r for r in TABLE_ROWS if r[0] in args.table_only.split(",")]
+    for name, thr in rows:
+        w = W.WORKLOADS[name]
+        if name not in cache:
+            cache.clear()
+            cache[name] = W.generate(w, seed=0)
+        data = cache[name]
+        q, k, v = (nabla.from_storage(data[n], dev) for n in "qkv")
+        sta = nabla.nabla_sta_mask(*w.grid, *w.sta_half_widths, device=dev)
+        kv_nb = torch.empty((w.B, w.h, w.s1), dtype=torch.int32, device=dev)
+        kv_inds = torch.empty((w.B, w.h, w.s1, w.s1), dtype=torch.int32, device=dev)
+        ws = torch.empty(nabla.nabla_build_mask_workspace_bytes(w.B, w.S, w.h, w.D),
+                         dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        for _ in range(max(3, args.warmup)):
+            nabla.nabla_build_mask(q, k, sta, thr, kv_nb, kv_inds, ws)
+            nabla.nabla_attn_fwd(q, k, v, kv_nb, kv_inds, w.scale, o)
+        torch.cuda.synchronize()
+        steps = args.steps
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        with ClockSampler(gpu_id(dev)) as clocks:
+            for s in range(steps):
+                ev[s][0].record(stream)
+                nabla.nabla_build_mask(q, k, sta, thr, kv_nb, kv_inds, ws)
+                ev[s][1].record(stream)
+                nabla.nabla_attn_fwd(q, k, v, kv_nb, kv_inds, w.scale, o)
+                ev[s][2].record(stream)
+            torch.cuda.synchronize()
+        assert nabla.nabla_get_last_device_status() == 0
+        mask_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+        attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+        kept = int(kv_nb.sum().item())
+        mask_gbs = mask_bytes(w, kept) / (mask_ms * 1e-3) / 1e9
+        kept_tf = attn_flops(w, kept) / (attn_ms * 1e-3) / 1e12
+        l2 = "inputs larger than L2, no flush" if q.numel() * q.element_size() > 129e6 else \
+            "inputs smaller than L2: back-to-back calls, not flushed (warm L2)"
+        row = {"workload": name, "thr": thr, "dtype": w.dtype, "density": kept / (
+                   w.B * w.h * w.s1 * w.s1), "kept_blocks": kept,
+               "mask_us": mask_ms * 1e3, "mask_gbs": mask_gbs,
+               "mask_frac_hbm": mask_gbs / peaks["hbm_gbs"],
+               "attn_ms": attn_ms, "attn_tflops_kept": kept_tf,
+               "attn_tflops_dense_equiv": dense_flops(w) / (attn_ms * 1e-3) / 1e12,
+               "attn_frac_bf16_sustained": kept_tf / peaks["bf16_tflops_sustained"],
+               "attn_frac_bf16_burst": kept_tf / peaks["bf16_tflops"],
+               "attn_path": "tcgen05 bf16" if w.dtype == "bf16" else "CUDA-core fp32",
+               "steps": steps, "l2": l2, "peaks": src, "clocks": clocks.summary()}
+        if not args.no_cpu_baseline:
+            row["cpu_baseline"] = table_cpu_leg(w, data, sta.cpu().numpy(), thr,
+                                                kv_nb.cpu().numpy(), kv_inds.cpu().numpy())
+        print(json.dumps(row), flush=True)
+        del q, k, v, kv_nb, kv_inds, ws, o
 
 
 def main():
@@ -532,7 +687,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-qblocks", type=int, default=8)
+    ap.add_argument("--table", action="store_true",
+                    help="one line per seeded configuration and sweep threshold")
+    ap.add_argument("--table-only", default="", help="comma-separated workloads of --table")
     args = ap.parse_args()
+    if args.table:
+        run_table(args)
+        return
     w = W.WORKLOADS[args.workload]
     thr = args.thr if args.thr is not None else w.thr[0]
     if args.impl == "reference":
