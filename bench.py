@@ -315,20 +315,6 @@ def run_ours(args, w, thr):
     mask_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
     assert nabla.nabla_get_last_device_status() == 0
-    # The same steps with nothing recorded between a step's mask build and its
-    # attention (one event pair around all K), as a user's loop runs them: the
-    # attention's launch and prologue then overlap the mask build's tail through
-    # the chained launches.  Timed after the region above, not part of `value`.
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    c0.record(stream)
-    for s in range(args.steps):
-        step()
-    c1.record(stream)
-    torch.cuda.synchronize()
-    chained_ms = c0.elapsed_time(c1) / args.steps
-    assert nabla.nabla_get_last_device_status() == 0
-
     total_ms, kept_all = reduce_over_ranks(dist, dev, total_ms, kept)
     ms_per_step = total_ms / args.steps
     value = whole_job_tflops(w, kept_all, total_ms, args.steps)
@@ -422,6 +408,20 @@ def run_ours(args, w, thr):
                "copies": "double-buffered on two copy streams, overlapping compute",
                "h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs, "clocks": e2e_clocks.summary()}
         del bufs
+
+    # The same steps with nothing recorded between a step's mask build and its
+    # attention (one event pair around all K), as a user's loop runs them: the
+    # attention's launch and prologue then overlap the mask build's tail through
+    # the chained launches.  Timed after the regions above, not part of `value`.
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(stream)
+    for s in range(args.steps):
+        step()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    chained_ms = c0.elapsed_time(c1) / args.steps
+    assert nabla.nabla_get_last_device_status() == 0
 
     # beside the step, timed on their own (not part of it): the steps either side
     # of the path, fractal flatten of a q-sized latent and its inverse, and the

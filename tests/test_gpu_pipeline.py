@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-import mask_tolerance as T
+import mask_tolerance as MT
 from block_sparse_attention_nablat_gb300 import workloads as W
 from oracle import nabla_oracle as O
 
@@ -60,8 +60,8 @@ def test_raster_layer_through_fractal_order(nabla):
     nbh, indh = nb.cpu().numpy(), inds.cpu().numpy()
     got = _mask_of(nbh, indh, w.s1)
     sta_h = O.sta_mask(*w.grid, 1, 1, 1)
-    theta = T.block_margins(of["q"], of["k"], ref["p"])
-    amb = O.ambiguous_blocks(ref["c"], ref["t"], sta_h) | T.near_tie_blocks(
+    theta = MT.block_margins(of["q"], of["k"], ref["p"])
+    amb = O.ambiguous_blocks(ref["c"], ref["t"], sta_h) | MT.near_tie_blocks(
         ref["p"], ref["cdf_mask"], theta, sta_h)
     assert np.array_equal(got[~amb], ref["mask"][~amb])
     oref = O.block_sparse_attention(of["q"], of["k"], of["v"], nbh, indh, w.scale)
