@@ -33,18 +33,29 @@
 //    entry's two membership bits in entry order (so the softmax threads read one
 //    16-bit pair per step instead of each scanning the bitmaps) and issues
 //    the TMA loads of Q (once per unit) and of the K pair slots, warp 3 those of
-//    the per-entry V tiles (two producers, so a wait for a V slot never holds
-//    back the next K pair); one thread of warp 1 issues every QK^T and one
-//    thread of warp 2 every PV (two issue streams, so one stream's waits never
-//    leave the tensor pipe without queued work); warps 4-7 and 8-11 are two
+//    the V tiles of each step into a V pair slot (two producers, so a wait for
+//    a V slot never holds back the next K pair); one thread of warp 1 issues
+//    every QK^T and one thread of warp 2 every PV (two issue streams, so one
+//    stream's waits never leave the tensor pipe without queued work).
+//  * The issuing threads, not the tensor pipe, set the step time: a step's 16
+//    MMAs take 1024 cycles when issued back to back, but every mbarrier wait,
+//    tcgen05.commit and fence on an issuing thread's path costs it hundreds of
+//    cycles.  So each issuer waits on two barriers and commits once per step:
+//    s_full, which the QK^T of step g commits, also frees K pair slot g % 3 for
+//    the K loader, and pv_done, which the PV of step g commits, also frees V
+//    pair slot g % 2 for the V loader.  Warps 4-7 and 8-11 are two
 //    softmax groups splitting each step's columns (group x takes entry x).
 //    Thread r of a group = TMEM lane r = query row r; the two threads of a row
-//    exchange their partial row max through shared memory every step (a
-//    barrier per warp pair), so both use one reference max and one O.
+//    exchange a flag through shared memory every step (a barrier per warp
+//    pair), so both keep one bias and one O.
 //  * Online softmax in base 2 with the scale folded in (packed f32x2 FMA for
-//    the exponent argument); the running max is raised (and O, l rescaled)
-//    only when it grows by more than 2^8, so the O correction through TMEM is
-//    rare; the result is exact either way since O and l share the max.
+//    the exponent argument).  The running maximum is only the exponent's bias:
+//    each step's P is computed with the bias as it stands, and only when the
+//    step's P sum exceeds 2^60 (or is infinite, for a row with no bias yet) do
+//    the two threads of the row compute the row maximum, rescale O and l through
+//    TMEM and redo the step.  Most steps thus need neither a row maximum nor a
+//    maximum exchange, only a one-flag exchange; the result is exact either way
+//    since O and l share the bias.
 //  * Every mbarrier wait is bounded (1 s); on expiry the kernel records
 //    NABLA_ERR_TIMEOUT, all roles stop waiting (the warp-pair barriers are
 //    still met in lockstep, so no partner is left behind), in-flight MMAs and
@@ -75,8 +86,9 @@ struct Cfg {
   static constexpr int kPairBox = 128 * 128;     // one 64-column box of a K pair slot (128 rows)
   static constexpr int kPairBytes = 2 * kTileBytes;
   static constexpr int kKStages = 3;             // K pair slots (steps)
-  static constexpr int kVStages = D == 128 ? 4 : 8;  // V tiles (entries)
+  static constexpr int kVPairs = 2;              // V pair slots (steps, two tiles each)
   static constexpr int kSBufs = 3;
+  static_assert(kKStages == kSBufs, "a K pair slot is freed by its step's s_full");
   static constexpr uint32_t kSCol = 128;         // score buffer b at TMEM columns 128 + 128 b
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescQK2 = idesc_bf16(128, 128, 0, 0);
@@ -87,17 +99,18 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kPairBytes;
-  static constexpr int kOffInfo = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffInfo = kOffV + kVPairs * kPairBytes;
   static constexpr int kOffXmax = kOffInfo + 2 * (int)sizeof(UnitInfo);  // [2 parity][2 grp][128]
   static constexpr int kOffXl = kOffXmax + 2 * 2 * 128 * 4;             // [2 grp][128]
-  static constexpr int kOffFlags = kOffXl + 2 * 128 * 4;                // [2 unit buffers][kMaxEntries]
+  static constexpr int kOffXslow = kOffXl + 2 * 128 * 4;                // [2 grp][128]
+  static constexpr int kOffFlags = kOffXslow + 2 * 128 * 4;             // [2 unit buffers][kMaxEntries]
   static constexpr int kOffBars = kOffFlags + 2 * kMaxEntries;
 };
 
 // All mbarriers and small shared flags, laid out by the compiler (8-byte aligned).
 template <int NK, int NV, int NS>
 struct SharedSync {
-  uint64_t k_full[NK], k_empty[NK], v_full[NV], v_empty[NV];
+  uint64_t k_full[NK], v_full[NV];
   uint64_t q_full, q_empty, info_full[2], info_empty[2];
   uint64_t s_full[NS], p_full[NS], pv_done[NS];
   uint64_t o_free, drain;
@@ -106,7 +119,7 @@ struct SharedSync {
 };
 
 template <int D>
-using SyncOf = SharedSync<Cfg<D>::kKStages, Cfg<D>::kVStages, Cfg<D>::kSBufs>;
+using SyncOf = SharedSync<Cfg<D>::kKStages, Cfg<D>::kVPairs, Cfg<D>::kSBufs>;
 
 template <int D>
 constexpr int smem_bytes() {
@@ -116,8 +129,8 @@ static_assert(smem_bytes<128>() <= 232448, "shared memory budget (D=128)");
 static_assert(smem_bytes<64>() <= 232448, "shared memory budget (D=64)");
 
 struct Bars {
-  uint64_t *k_full, *k_empty, *v_full, *v_empty, *q_full, *q_empty, *info_full, *info_empty,
-      *s_full, *p_full, *pv_done, *o_free, *drain;
+  uint64_t *k_full, *v_full, *q_full, *q_empty, *info_full, *info_empty, *s_full, *p_full,
+      *pv_done, *o_free, *drain;
 };
 
 
@@ -148,10 +161,9 @@ __device__ __forceinline__ void sm_arrive(uint64_t *bar, int lane) {
 }
 
 // P for 32 scores: 2^(s * scale_log2 - m) in fp32 (row-sum accumulators updated),
-// packed to bf16 pairs and stored over 16 TMEM columns at taddr.
-__device__ __forceinline__ void exp_pack_store(const uint32_t (&r)[32], uint64_t sc2, uint64_t nm2,
-                                               uint64_t &acc0, uint64_t &acc1, uint32_t taddr) {
-  uint32_t pk[16];
+// packed to bf16 pairs in pk (16 TMEM columns' worth).
+__device__ __forceinline__ void exp_pack(const uint32_t (&r)[32], uint64_t sc2, uint64_t nm2,
+                                         uint64_t &acc0, uint64_t &acc1, uint32_t (&pk)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
     float x0, x1, y0, y1;
@@ -167,20 +179,47 @@ __device__ __forceinline__ void exp_pack_store(const uint32_t (&r)[32], uint64_t
     pk[i] = pack_bf16x2(x0, x1);
     pk[i + 1] = pack_bf16x2(y0, y1);
   }
-  tmem_st16(taddr, pk);
 }
+
+// Row maximum of 64 scores times scale_log2 (the minimum for a negative scale).
+__device__ __forceinline__ float scaled_row_max(const uint32_t (&r0)[32], const uint32_t (&r1)[32],
+                                                float sl2) {
+  float a0, a1, a2, a3;
+  if (sl2 >= 0.f) {
+    a0 = a1 = a2 = a3 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      a0 = max3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+      a1 = max3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+      a2 = max3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+      a3 = max3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+    }
+    a0 = max3(a0, a1, fmaxf(a2, a3));
+  } else {
+    a0 = a1 = a2 = a3 = INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      a0 = min3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+      a1 = min3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+      a2 = min3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
+      a3 = min3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
+    }
+    a0 = min3(a0, a1, fminf(a2, a3));
+  }
+  return a0 * sl2;
+}
+
+// A step's P is used as computed with the running maximum unless its sum exceeds
+// this (then some P is huge, or the row had no maximum yet and P is infinite).
+constexpr float kPBig = 1.152921504606846976e18f;  // 2^60
 
 // On the abort path: wait (bounded, ignoring the abort flag) until the last
 // copies this thread issued have landed, so none writes shared memory after exit.
 template <int D>
-__device__ void drain_copies(const Params &P, const Bars &bar, uint32_t gk, uint32_t ge,
-                             uint32_t kq) {
+__device__ void drain_copies(const Params &P, const Bars &bar, uint32_t gk, uint32_t kq) {
   using C = Cfg<D>;
   for (uint32_t e = gk > (uint32_t)C::kKStages ? gk - C::kKStages : 0u; e < gk; ++e)
     mbar_wait(&bar.k_full[e % C::kKStages], (e / C::kKStages) & 1u, nullptr, P.status,
-              kDevTimeout);
-  for (uint32_t e = ge > (uint32_t)C::kVStages ? ge - C::kVStages : 0u; e < ge; ++e)
-    mbar_wait(&bar.v_full[e % C::kVStages], (e / C::kVStages) & 1u, nullptr, P.status,
               kDevTimeout);
   if (kq > 0) mbar_wait(bar.q_full, (kq - 1) & 1u, nullptr, P.status, kDevTimeout);
 }
@@ -196,7 +235,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
   const int lane = threadIdx.x & 31;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
-  uint32_t gk = 0, ge = 0, kq = 0;  // K pair slots issued, (V: none here), Q tiles issued
+  uint32_t gk = 0, kq = 0;  // K pair slots issued, Q tiles issued
   bool stop = false;  // lane 0: a wait gave up; every lane leaves together at the loop top
   int k = 0;
   for (long u = blockIdx.x; u < units; u += gridDim.x, ++k) {
@@ -264,8 +303,11 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     Cursor ck{0, inf.a[0] | inf.b[0]};
     bool go = true;
     auto load_k = [&](int s) {  // both entries of step s into one pair slot
+      // pair slot gk % 3 is free once the QK^T of step gk - 3 is done, which is
+      // the completion s_full[gk % 3] signals (K slots and score buffers share
+      // the step index)
       const uint32_t ks = gk % C::kKStages;
-      go = go && mbar_wait(&bar.k_empty[ks], ((gk / C::kKStages) & 1) ^ 1, abort, P.status,
+      go = go && mbar_wait(&bar.s_full[ks], ((gk / C::kKStages) & 1) ^ 1, abort, P.status,
                            kDevTimeout);
       if (!go) return;
       const int ne = (2 * s + 1 < cnt) ? 2 : 1;
@@ -287,17 +329,21 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     }
     if (!go) stop = true;
   }
-  if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, ge, kq);
+  if (lane == 0 && (stop || *abort)) drain_copies<D>(P, bar, gk, kq);
 }
 
-// Warp 3, lane 0: the V tile of every entry, in entry order, into the V ring.
+// Warp 3, lane 0: the V tiles of every step (its one or two entries, in entry
+// order) into a V pair slot.  Pair slot g % 2 is free once the PV of step g - 2
+// is done: the V loader waits on that step's pv_done, so the PV issuer spends
+// one wait and one commit per step on V, not two of each.
 template <int D>
 __device__ void v_producer(const Params &P, const CUtensorMap *tmV, uint8_t *smem,
                            UnitInfo *info, const Bars &bar, volatile int *abort) {
   using C = Cfg<D>;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
-  uint32_t ge = 0;
+  static_assert(C::kVPairs < C::kSBufs, "pv_done of step g - kVPairs cannot have moved on");
+  uint32_t gv = 0;  // steps loaded
   bool go = true;
   int k = 0;
   for (long u = blockIdx.x; u < units && go && !*abort; u += gridDim.x, ++k) {
@@ -310,26 +356,32 @@ __device__ void v_producer(const Params &P, const CUtensorMap *tmV, uint8_t *sme
     const int n = inf.n;
     const Unit un = decode(u, npairs, P.h);
     Cursor cv{0, inf.a[0] | inf.b[0]};
-    for (int e = 0; e < n && go; ++e) {
-      const uint32_t vs = ge % C::kVStages;
-      go = mbar_wait(&bar.v_empty[vs], ((ge / C::kVStages) & 1) ^ 1, abort, P.status,
-                     kDevTimeout);
-      if (!go) break;
-      uint32_t fl;
-      const int j = next_entry(inf, cv, fl);
-      mbar_expect_tx(&bar.v_full[vs], C::kTileBytes);
+    for (int e = 0; e < n && go; e += 2) {
+      const uint32_t vp = gv % C::kVPairs;
+      if (gv >= (uint32_t)C::kVPairs) {
+        const uint32_t gp = gv - C::kVPairs;
+        go = mbar_wait(&bar.pv_done[gp % C::kSBufs], (gp / C::kSBufs) & 1u, abort, P.status,
+                       kDevTimeout);
+        if (!go) break;
+      }
+      const int ne = e + 1 < n ? 2 : 1;
+      mbar_expect_tx(&bar.v_full[vp], ne * C::kTileBytes);
+      for (int x = 0; x < ne; ++x) {
+        uint32_t fl;
+        const int j = next_entry(inf, cv, fl);
 #pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c)
-        tma_load_4d(smem + C::kOffV + vs * C::kTileBytes + c * 64 * 128, tmV, &bar.v_full[vs],
-                    c * 64, un.hh, j * 64, un.b);
-      ++ge;
+        for (int c = 0; c < C::kBoxes; ++c)
+          tma_load_4d(smem + C::kOffV + (vp * 2 + x) * C::kTileBytes + c * 64 * 128, tmV,
+                      &bar.v_full[vp], c * 64, un.hh, j * 64, un.b);
+      }
+      ++gv;
     }
     if (!go) break;
     mbar_arrive(&bar.info_empty[ub]);
   }
   if (!go || *abort)  // let in-flight copies land before the CTA exits
-    for (uint32_t e = ge > (uint32_t)C::kVStages ? ge - C::kVStages : 0u; e < ge; ++e)
-      mbar_wait(&bar.v_full[e % C::kVStages], (e / C::kVStages) & 1u, nullptr, P.status,
+    for (uint32_t e = gv > (uint32_t)C::kVPairs ? gv - C::kVPairs : 0u; e < gv; ++e)
+      mbar_wait(&bar.v_full[e % C::kVPairs], (e / C::kVPairs) & 1u, nullptr, P.status,
                 kDevTimeout);
 }
 
@@ -376,7 +428,7 @@ __device__ void qk_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const 
           const uint64_t bd = kd + (uint64_t)((((kk >> 2) * C::kPairBox) + (kk & 3) * 32) >> 4);
           mma_ss(d, a, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&bar.k_empty[ks.slot]);  // K pair slot reusable once this QK^T is done
+        // s_full also frees K pair slot ks (= sb: both rings count steps) for the loader
         mma_commit(&bar.s_full[sb.slot]);
         if (s + 1 == steps) mma_commit(bar.q_empty);  // Q reusable after the unit's last QK^T
         sb.next();
@@ -402,7 +454,7 @@ __device__ void pv_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const 
   const long units = (long)P.B * P.h * npairs;
   const uint64_t v_desc = smem_desc_sw128(smem_u32(smem + C::kOffV), 64 * 128, 1024);
   Ring<C::kSBufs> sb;
-  Ring<C::kVStages> vs;
+  Ring<C::kVPairs> vp;  // V pair slot of the next step
   uint32_t kq = 0;
   int k = 0;
   bool ok = true;
@@ -415,25 +467,22 @@ __device__ void pv_issuer(const Params &P, uint8_t *smem, UnitInfo *info, const 
       // O of the previous unit must have been read out before the first PV overwrites it
       if (kq > 0 && !mbar_wait(bar.o_free, (kq - 1) & 1u, abort, P.status, kDevTimeout)) break;
       for (int s = 0; s < steps; ++s) {
-        ok = mbar_wait(&bar.p_full[sb.slot], sb.phase, abort, P.status, kDevTimeout);
+        ok = mbar_wait(&bar.p_full[sb.slot], sb.phase, abort, P.status, kDevTimeout) &&
+             mbar_wait(&bar.v_full[vp.slot], vp.phase, abort, P.status, kDevTimeout);
         if (!ok) break;
         tc_fence_after();
         for (int x = 0; x < 2 && 2 * s + x < n; ++x) {
-          ok = mbar_wait(&bar.v_full[vs.slot], vs.phase, abort, P.status, kDevTimeout);
-          if (!ok) break;
-          tc_fence_after();
-          const uint64_t vd = v_desc + (uint64_t)((vs.slot * C::kTileBytes) >> 4);
+          const uint64_t vd = v_desc + (uint64_t)(((vp.slot * 2 + x) * C::kTileBytes) >> 4);
           const uint32_t a0 = tmem + C::kSCol + sb.slot * 128 + x * 64;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tmem, a0 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), C::kIdescPV,
                    (s > 0 || x > 0 || kk > 0) ? 1u : 0u);  // next 16 KV rows
-          mma_commit(&bar.v_empty[vs.slot]);
-          vs.next();
         }
-        if (!ok) break;
+        // frees score buffer sb for QK^T and V pair slot vp for the V loader
         mma_commit(&bar.pv_done[sb.slot]);
         sb.next();
+        vp.next();
       }
       if (!ok) break;
       ++kq;
@@ -457,10 +506,10 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
   const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
   float *xmax = reinterpret_cast<float *>(smem + C::kOffXmax);
   float *xl = reinterpret_cast<float *>(smem + C::kOffXl);
+  float *xslow = reinterpret_cast<float *>(smem + C::kOffXslow);
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   const float sl2 = P.scale_log2;
-  const bool pos_scale = sl2 >= 0.f;
   uint32_t gs = 0;
   int k = 0;
   bool live = true;  // false after a wait gave up: keep meeting the pair barriers, do no work
@@ -494,84 +543,77 @@ __device__ void softmax_epilogue(const Params &P, UnitInfo *info, uint8_t *smem,
       tc_fence_after();
       const uint32_t sbase = tmem + lane_base + C::kSCol + b * 128 + grp * 64;
       uint32_t r0[32], r1[32];
-      float mx = -INFINITY;
       if (live && act) {
         tmem_ld32(sbase, r0);
         tmem_ld32(sbase + 32, r1);
         tmem_wait_ld();
         reg_fence(r0);
         reg_fence(r1);
-        float a0, a1, a2, a3;
-        if (pos_scale) {
-          a0 = a1 = a2 = a3 = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            a0 = max3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-            a1 = max3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
-            a2 = max3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
-            a3 = max3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
-          }
-          a0 = max3(a0, a1, fmaxf(a2, a3));
-        } else {
-          a0 = a1 = a2 = a3 = INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            a0 = min3(a0, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-            a1 = min3(a1, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
-            a2 = min3(a2, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
-            a3 = min3(a3, __uint_as_float(r1[i + 2]), __uint_as_float(r1[i + 3]));
-          }
-          a0 = min3(a0, a1, fminf(a2, a3));
-        }
-        mx = a0 * sl2;
       }
-      // exchange the partial row max with the partner thread (same row, other group)
+      // P with the running maximum as it stands.  The maximum only serves as the
+      // exponent's bias, and the result is exact for any bias that keeps P finite,
+      // so it is raised only when this step's P would be huge (or infinite: a row
+      // with no maximum yet).  The two threads of a row agree on that through the
+      // exchange slot, and only then compute the row maximum, rescale O and l,
+      // and redo the step's P.
+      uint32_t pk0[16], pk1[16];
+      float ssum = 0.f;
+      auto step_p = [&]() {
+        const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_run, -m_run);
+        uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;
+        exp_pack(r0, sc2, nm2, acc0, acc1, pk0);
+        exp_pack(r1, sc2, nm2, acc0, acc1, pk1);
+        float s0, s1v, s2, s3;
+        unf2(acc0, s0, s1v);
+        unf2(acc1, s2, s3);
+        ssum = (s0 + s1v) + (s2 + s3);
+      };
+      if (live && act) step_p();
+      const bool big = !(ssum <= kPBig);  // also for an infinite or NaN sum
       float *xm = xmax + (size_t)(g & 1u) * 2 * 128;
-      xm[grp * 128 + row] = mx;
+      xm[grp * 128 + row] = big ? 1.f : 0.f;
       pair_sync(q4);
-      const float m_new = fmaxf(m_run, fmaxf(mx, xm[(grp ^ 1) * 128 + row]));
-      const bool any_row = m_new != -INFINITY;  // some block kept for this row so far
-      const bool resc = m_run != -INFINITY && m_new > m_run + 8.0f;
-      if (__any_sync(0xffffffffu, resc)) {
-        // O must hold every PV up to the previous step before it is rescaled;
-        // each group rescales its half of the D columns (the decision is the same
-        // in both groups, both hold the same m_run)
-        const uint32_t gp = g - 1;
-        const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
-        live = __all_sync(0xffffffffu,
-                          live && mbar_wait(&bar.pv_done[gp % C::kSBufs], (gp / C::kSBufs) & 1u,
-                                            abort, P.status, kDevTimeout));
-        if (live) {
-          tc_fence_after();
+      const bool need = big || xm[(grp ^ 1) * 128 + row] != 0.f;
+      if (__any_sync(0xffffffffu, need)) {
+        const float mx = (need && live && act) ? scaled_row_max(r0, r1, sl2) : -INFINITY;
+        xslow[grp * 128 + row] = mx;
+        pair_sync(q4);
+        const float m_new = need ? fmaxf(m_run, fmaxf(mx, xslow[(grp ^ 1) * 128 + row])) : m_run;
+        const bool resc = need && m_run != -INFINITY && m_new > m_run;
+        if (__any_sync(0xffffffffu, resc)) {
+          // O must hold every PV up to the previous step before it is rescaled;
+          // each group rescales its half of the D columns (the decision is the same
+          // in both groups, both hold the same m_run)
+          const uint32_t gp = g - 1;
+          const float alpha = resc ? ex2(m_run - m_new) : 1.0f;
+          live = __all_sync(0xffffffffu,
+                            live && mbar_wait(&bar.pv_done[gp % C::kSBufs], (gp / C::kSBufs) & 1u,
+                                              abort, P.status, kDevTimeout));
+          if (live) {
+            tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            const uint32_t ta = tmem + lane_base + grp * (D / 2) + c * 16;
-            uint32_t t[16];
-            tmem_ld16(ta, t);
-            tmem_wait_ld();
-            reg_fence16(t);
+            for (int c = 0; c < D / 32; ++c) {
+              const uint32_t ta = tmem + lane_base + grp * (D / 2) + c * 16;
+              uint32_t t[16];
+              tmem_ld16(ta, t);
+              tmem_wait_ld();
+              reg_fence16(t);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
-            tmem_st16(ta, t);
+              for (int i = 0; i < 16; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+              tmem_st16(ta, t);
+            }
+            tmem_wait_st();
           }
-          tmem_wait_st();
+          if (resc) l_run *= alpha;
         }
-        if (resc) {
-          l_run *= alpha;
-          m_run = m_new;
-        }
+        if (need) m_run = m_new;
+        if (need && live && act) step_p();
       }
-      if (m_run == -INFINITY && any_row) m_run = m_new;
       if (live && mine) {
         if (act) {
-          const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-m_run, -m_run);
-          uint64_t acc0 = f2(0.f, 0.f), acc1 = acc0;
-          exp_pack_store(r0, sc2, nm2, acc0, acc1, sbase);
-          exp_pack_store(r1, sc2, nm2, acc0, acc1, sbase + 16);
-          float s0, s1v, s2, s3;
-          unf2(acc0, s0, s1v);
-          unf2(acc1, s2, s3);
-          l_run += (s0 + s1v) + (s2 + s3);
+          tmem_st16(sbase, pk0);
+          tmem_st16(sbase + 16, pk1);
+          l_run += ssum;
         } else {
           uint32_t pk[16];
 #pragma unroll
@@ -649,9 +691,7 @@ __global__ void __launch_bounds__(384, 1)
   SyncOf<D> *sync = reinterpret_cast<SyncOf<D> *>(smem + C::kOffBars);
   Bars bar;
   bar.k_full = sync->k_full;
-  bar.k_empty = sync->k_empty;
   bar.v_full = sync->v_full;
-  bar.v_empty = sync->v_empty;
   bar.q_full = &sync->q_full;
   bar.q_empty = &sync->q_empty;
   bar.info_full = sync->info_full;
@@ -667,14 +707,8 @@ __global__ void __launch_bounds__(384, 1)
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kKStages; ++i) {
-      mbar_init(&bar.k_full[i], 1);
-      mbar_init(&bar.k_empty[i], 1);
-    }
-    for (int i = 0; i < C::kVStages; ++i) {
-      mbar_init(&bar.v_full[i], 1);
-      mbar_init(&bar.v_empty[i], 1);
-    }
+    for (int i = 0; i < C::kKStages; ++i) mbar_init(&bar.k_full[i], 1);
+    for (int i = 0; i < C::kVPairs; ++i) mbar_init(&bar.v_full[i], 1);
     mbar_init(bar.q_full, 1);
     mbar_init(bar.q_empty, 1);
     for (int i = 0; i < 2; ++i) {
