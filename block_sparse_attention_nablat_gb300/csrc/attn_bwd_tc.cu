@@ -84,8 +84,7 @@ struct BCfg {
 struct BSync {
   uint64_t st_full[4], st_empty[4];
   uint64_t a_full, a_empty, info_full[2], info_empty[2];
-  uint64_t s_full[2], x_read[2], p_full[2], buf_free[2];  // buf_free: dz buffer (dQ) or
-                                                          // X / Y buffer (dK/dV) read by TS
+  uint64_t s_full[2], x_read[2], p_full[2];
   uint64_t acc_full, acc_free, drain;
   uint32_t tmem_slot;
   int abort;
@@ -248,9 +247,14 @@ __device__ void b_ss(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy
         const uint32_t st = ge % C::kStages;
         const uint32_t b = g & 1u;
         ok = mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u, abort, P.status, kDevTimeout);
-        if (ok && g >= 2)
-          ok = mbar_wait(kDQ ? &sy->x_read[b] : &sy->buf_free[b], ((g >> 1) - 1) & 1u, abort,
-                         P.status, kDevTimeout);
+        if (ok && g >= 2) {
+          // dQ: the softmax of step g-2 has read X / Y; dK/dV: the TS MMAs of step g-2,
+          // whose completion st_empty[(g-2) % 4] signals, have read the P / dz over them
+          const uint32_t g2 = g - 2;
+          ok = kDQ ? mbar_wait(&sy->x_read[b], ((g >> 1) - 1) & 1u, abort, P.status, kDevTimeout)
+                   : mbar_wait(&sy->st_empty[g2 % C::kStages], (g2 / C::kStages) & 1u, abort,
+                               P.status, kDevTimeout);
+        }
         if (!ok) break;
         tc_fence_after();
         const uint64_t t1 = tk_desc + (uint64_t)((st * C::kStageBytes) >> 4);
@@ -317,9 +321,9 @@ __device__ void b_ts(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy
           }
         }
         // the stage (read by both streams; SS(g) finished before the softmax of
-        // step g began) and the P / dz of buffer b are free once these are done
+        // step g began) and the P / dz of buffer b are free once these are done:
+        // one commit signals both (the stage ring and the steps count alike)
         mma_commit(&sy->st_empty[st]);
-        mma_commit(&sy->buf_free[b]);
       }
       if (!ok) break;
       mma_commit(&sy->acc_full);
@@ -415,10 +419,14 @@ __device__ void b_softmax(const TcParams &P, uint8_t *smem, UnitInfo *info, BSyn
       if (kDQ) {
         tc_fence_before();
         mbar_arrive(&sy->x_read[b]);  // buffer b may take the products of step g + 2
-        // the dz buffer of step g was last read by the TS MMAs of step g - 2
-        if (g >= 2)
-          live = __all_sync(0xffffffffu, mbar_wait(&sy->buf_free[b], ((g >> 1) - 1) & 1u, abort,
-                                                   P.status, kDevTimeout));
+        // the dz buffer of step g was last read by the TS MMAs of step g - 2, whose
+        // completion st_empty[(g - 2) % 4] signals
+        if (g >= 2) {
+          const uint32_t g2 = g - 2;
+          live = __all_sync(0xffffffffu, mbar_wait(&sy->st_empty[g2 % C::kStages],
+                                                   (g2 / C::kStages) & 1u, abort, P.status,
+                                                   kDevTimeout));
+        }
         if (!live) break;
         tc_fence_after();
         const uint32_t pd = tmem + lane_base + C::kPD + b * 64;
@@ -505,7 +513,6 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sy->info_full[i], 1);
       mbar_init(&sy->info_empty[i], C::kSoftmax + 2);  // softmax threads + both MMA issuers
       mbar_init(&sy->p_full[i], C::kSoftmax);
-      mbar_init(&sy->buf_free[i], 1);
       mbar_init(&sy->s_full[i], 1);
       mbar_init(&sy->x_read[i], C::kSoftmax);
     }
