@@ -82,7 +82,7 @@ struct BCfg {
 };
 
 struct BSync {
-  uint64_t st_full[4], st_empty[4];
+  uint64_t st_full[4], st_empty[4], x_free[4];  // x_free: dK/dV, the TS MMAs that read P are done
   uint64_t a_full, a_empty, info_full[2], info_empty[2];
   uint64_t s_full[2], x_read[2], p_full[2];
   uint64_t acc_full, acc_free, drain;
@@ -247,24 +247,35 @@ __device__ void b_ss(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy
         const uint32_t st = ge % C::kStages;
         const uint32_t b = g & 1u;
         ok = mbar_wait(&sy->st_full[st], (ge / C::kStages) & 1u, abort, P.status, kDevTimeout);
-        if (ok && g >= 2) {
-          // dQ: the softmax of step g-2 has read X / Y; dK/dV: the TS MMAs of step g-2,
-          // whose completion st_empty[(g-2) % 4] signals, have read the P / dz over them
-          const uint32_t g2 = g - 2;
+        const uint32_t g2 = g - 2;
+        // dQ: the softmax of step g-2 has read X / Y.  dK/dV: P and dz of step g-2 sit
+        // over X and Y; X may be rewritten once the TS MMAs that read P (dV) are done
+        // (x_free), Y once those that read dz (dK) are done too (st_empty)
+        if (ok && g >= 2)
           ok = kDQ ? mbar_wait(&sy->x_read[b], ((g >> 1) - 1) & 1u, abort, P.status, kDevTimeout)
-                   : mbar_wait(&sy->st_empty[g2 % C::kStages], (g2 / C::kStages) & 1u, abort,
+                   : mbar_wait(&sy->x_free[g2 % C::kStages], (g2 / C::kStages) & 1u, abort,
                                P.status, kDevTimeout);
-        }
         if (!ok) break;
         tc_fence_after();
         const uint64_t t1 = tk_desc + (uint64_t)((st * C::kStageBytes) >> 4);
         const uint64_t t2 = tk_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
+        const uint32_t xb = tmem + C::kXY + b * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t da = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
           const uint64_t dt = (uint64_t)((((kk >> 2) * 64 * 128) + (kk & 3) * 32) >> 4);
-          const uint32_t xb = tmem + C::kXY + b * 128;
-          mma_ss(xb, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);       // X = A1 T1^T
+          mma_ss(xb, a1_desc + da, t1 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // X = A1 T1^T
+        }
+        if (!kDQ && g >= 2) {
+          ok = mbar_wait(&sy->st_empty[g2 % C::kStages], (g2 / C::kStages) & 1u, abort, P.status,
+                         kDevTimeout);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t da = (uint64_t)((((kk >> 2) * 128 * 128) + (kk & 3) * 32) >> 4);
+          const uint64_t dt = (uint64_t)((((kk >> 2) * 64 * 128) + (kk & 3) * 32) >> 4);
           mma_ss(xb + 64, a2_desc + da, t2 + dt, C::kIdSS, kk > 0 ? 1u : 0u);  // Y = A2 T2^T
         }
         mma_commit(&sy->s_full[b]);
@@ -308,16 +319,28 @@ __device__ void b_ts(const TcParams &P, uint8_t *smem, UnitInfo *info, BSync *sy
         tc_fence_after();
         const uint64_t t1 = tm_desc + (uint64_t)((st * C::kStageBytes) >> 4);
         const uint64_t t2 = tm_desc + (uint64_t)((st * C::kStageBytes + C::kTileBytes) >> 4);
+        if (kDQ) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
-          const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
-          const uint32_t acc = (e > 0 || kk > 0) ? 1u : 0u;
-          if (kDQ) {
+          for (int kk = 0; kk < 4; ++kk) {  // 16 entry rows per MMA
+            const uint64_t dk = (uint64_t)((kk * 16 * 128) >> 4);
+            const uint32_t acc = (e > 0 || kk > 0) ? 1u : 0u;
             mma_ts(tmem + C::kAcc1, tmem + C::kPD + b * 64 + kk * 8, t1 + dk, C::kIdTS, acc);
-          } else {  // entries 32 g .. 32 g + 31 sit at columns 32 g .. 32 g + 15 of X and Y
+          }
+        } else {
+          // entries 32 g .. 32 g + 31 sit at columns 32 g .. 32 g + 15 of X and Y; the
+          // MMAs that read P (in X) go first, so that X is free again sooner
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
             const uint32_t xb = tmem + C::kXY + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
-            mma_ts(tmem + C::kAcc0, xb, t2 + dk, C::kIdTS, acc);       // dV += P^T dout
-            mma_ts(tmem + C::kAcc1, xb + 64, t1 + dk, C::kIdTS, acc);  // dK += dz^T q
+            mma_ts(tmem + C::kAcc0, xb, t2 + (uint64_t)((kk * 16 * 128) >> 4), C::kIdTS,
+                   (e > 0 || kk > 0) ? 1u : 0u);  // dV += P^T dout
+          }
+          mma_commit(&sy->x_free[st]);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t xb = tmem + C::kXY + b * 128 + (kk >> 1) * 32 + (kk & 1) * 8;
+            mma_ts(tmem + C::kAcc1, xb + 64, t1 + (uint64_t)((kk * 16 * 128) >> 4), C::kIdTS,
+                   (e > 0 || kk > 0) ? 1u : 0u);  // dK += dz^T q
           }
         }
         // the stage (read by both streams; SS(g) finished before the softmax of
@@ -506,6 +529,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&sy->st_full[i], 1);
       mbar_init(&sy->st_empty[i], 1);
+      mbar_init(&sy->x_free[i], 1);
     }
     mbar_init(&sy->a_full, 1);
     mbar_init(&sy->a_empty, 1);
