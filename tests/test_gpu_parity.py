@@ -444,6 +444,57 @@ def test_hand_made_csr_edge_rows(nabla, dtype):
     assert np.all(o[0, 0:64, 0] == 0) and np.all(o[0, 7 * 64:8 * 64, 0] == 0)
 
 
+def _jump_inputs(jumps, seed=11):
+    """bf16 q, k, v (B=1, h=2, D=128, s1=8) whose logits jump along the key axis:
+    every query row gets a common component 8 u (u = the first unit vector) and key
+    block j of head hh gets c u for each (hh, j, c) in jumps, so that a row's scaled
+    base-2 logits against block j rise by about 0.1275 * q_0 * c, q_0 = 8 + noise.
+    With c = 100 every row's rise is 60 or more, past the kernel's 2^60 overflow
+    test; with c = 60 only some rows pass it, and the others stay on the fast path
+    with P values up to about 2^55."""
+    w = W.custom("jump", 1, 2, 128, 64 * 8, (8, 1, 1))
+    d = W.generate(w, seed)
+    qf, kf, vf = (W.as_float(d[n]).copy() for n in "qkv")
+    qf[..., 0] += 8.0
+    for hh, j, c in jumps:
+        kf[0, j * 64:(j + 1) * 64, hh, 0] += c
+    data = {"q": W.f32_to_bf16_bits(qf), "k": W.f32_to_bf16_bits(kf),
+            "v": W.f32_to_bf16_bits(vf)}
+    return w, data
+
+
+@pytest.mark.parametrize("jumps,partial", [
+    ([(0, 5, 100.0), (1, 2, 100.0)], False),  # one jump, in the second / first entry of a step
+    ([(0, 3, 100.0), (0, 6, 200.0), (1, 7, 100.0)], False),  # two jumps in a row; the last block
+    ([(0, 5, 100.0), (1, 4, 100.0)], True),  # only some query blocks keep the jumping block
+    ([(0, 5, 60.0), (1, 3, 60.0)], False),   # some rows rescale, the others keep big P values
+], ids=["one-jump", "two-jumps", "partial-rows", "mixed-rows"])
+def test_attention_rescale_path(nabla, jumps, partial):
+    """A key block whose logits exceed the running maximum by 2^60 or more makes the
+    kernel raise its exponent bias mid-row: O and l are rescaled through TMEM and the
+    step's P is redone.  Random inputs never reach that path.  The blocks before the
+    jump then carry 2^-60 or less of the weight, so an O or l left unscaled shows as an
+    O(1) error; output and lse are compared with the oracle on every row."""
+    w, data = _jump_inputs(jumps)
+    s1 = w.s1
+    mask = np.ones((1, 2, s1, s1), bool)
+    if partial:
+        mask[0, 0, 1::2, 5] = False   # odd query blocks of head 0 skip the jumping block
+        mask[0, 1, ::3, 4] = False
+    nb, inds = O.csr_from_mask(mask)
+    inds = np.where(inds < 0, 0, inds).astype(np.int32)
+    check_attention(nabla, w, data, nb, inds)
+    qkv = [nabla.from_storage(data[n], DEV) for n in "qkv"]
+    o, lse = nabla.nabla_attn_fwd_lse(*qkv, torch.from_numpy(nb).to(DEV),
+                                      torch.from_numpy(inds).to(DEV), w.scale)
+    assert nabla.nabla_get_last_device_status() == 0
+    qf, kf = W.as_float(data["q"]), W.as_float(data["k"])
+    ref = O.attention_lse2(qf, kf, nb, inds, w.scale)
+    got = lse.cpu().numpy().astype(np.float64)
+    # lse up to about 280: fp32 ulp 3e-5, plus the logits' fp32 accumulation
+    assert np.allclose(got, ref, rtol=0, atol=2e-3), float(np.abs(got - ref).max())
+
+
 def test_threshold_one_is_dense(nabla):
     """thr = 1 keeps every block, and the sparse attention equals dense attention."""
     w = W.custom("dense", 1, 2, 128, 64 * 48, (3, 4, 4), sigma=0.75, rho=0.8, thr=(1.0,))
