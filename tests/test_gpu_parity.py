@@ -495,6 +495,51 @@ def test_attention_rescale_path(nabla, jumps, partial):
     assert np.allclose(got, ref, rtol=0, atol=2e-3), float(np.abs(got - ref).max())
 
 
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 0.3])
+def test_attention_any_finite_scale(nabla, dtype, scale):
+    """The ABI takes any finite softmax scale.  A negative scale turns the row
+    maximum into a minimum of the raw scores (the kernel's sign-aware row maximum),
+    zero gives a uniform softmax over the kept tokens, and a large one sharpens it;
+    output and lse are compared with the oracle on every row."""
+    w = W.custom("scale", 1, 2, 64 if dtype == "f32" else 128, 64 * 12, (3, 2, 2), dtype=dtype)
+    data = inputs(w, seed=5)
+    s1 = w.s1
+    rng = np.random.default_rng(3)
+    mask = rng.random((1, 2, s1, s1)) < 0.5
+    mask[0, 0, 4] = False            # one empty row
+    nb, inds = O.csr_from_mask(mask)
+    inds = np.where(inds < 0, 0, inds).astype(np.int32)
+    qkv = [nabla.from_storage(data[n], DEV) for n in "qkv"]
+    o, lse = nabla.nabla_attn_fwd_lse(*qkv, torch.from_numpy(nb).to(DEV),
+                                      torch.from_numpy(inds).to(DEV), scale)
+    assert nabla.nabla_get_last_device_status() == 0
+    qf, kf, vf = (W.as_float(data[n]) for n in "qkv")
+    ref = oracle_attention(qf, kf, vf, nb, inds, scale)
+    err = np.abs(o.float().cpu().numpy() - ref)
+    if dtype == "f32":
+        assert err.max() <= TOL["f32"][0], err.max()
+    else:
+        # P enters the PV product as bf16 while l sums the fp32 weights: the numerator
+        # is off by at most 2^-9 sum_u p_u |v_u| / l <= 2^-9 max|v|; o is written as
+        # bf16, <= 2^-9 |o|; each logit carries the fp32 accumulation error of its dot
+        # product, at most delta = |scale| D 2^-24 max_su sum_i |q_si k_ui|, which
+        # moves every weight by a factor within e^(+-delta) and o by <= 2 delta max|v|.
+        # The fixed bounds of the other tests assume the default scale, whose flatter
+        # softmax averages these errors down.
+        vmax = float(np.abs(vf).max())
+        dot = max(float((np.abs(qf[b, :, hh]) @ np.abs(kf[b, :, hh]).T).max())
+                  for b in range(w.B) for hh in range(w.h))
+        delta = abs(scale) * w.D * 2.0 ** -24 * dot
+        bound = 2.0 ** -9 * (vmax + np.abs(ref)) + 2 * delta * vmax
+        assert np.all(err <= bound), float((err / bound).max())
+    lref = O.attention_lse2(qf, kf, nb, inds, scale)
+    got = lse.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(lref)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.allclose(got[fin], lref[fin], rtol=0, atol=1e-3), float(np.abs(got[fin] - lref[fin]).max())
+
 def test_threshold_one_is_dense(nabla):
     """thr = 1 keeps every block, and the sparse attention equals dense attention."""
     w = W.custom("dense", 1, 2, 128, 64 * 48, (3, 4, 4), sigma=0.75, rho=0.8, thr=(1.0,))
