@@ -43,9 +43,9 @@ METRIC = "NABLA attn fwd TFLOP/s on kept blocks (+dense-equiv); mask-build HBM G
 # captured: null.
 NCU_TRAFFIC = {
     "720p_bf16": {
-        "attention": {"bytes": 29.7771e9,
-                      "source": "ncu launch list, 720p, attn_tc_kernel with one wait pair "
-                                "and one commit per step on each MMA-issuing thread"},
+        "attention": {"bytes": 12.9557e9,
+                      "source": "ncu launch list, 720p, attn_tc_kernel with the "
+                                "entry-count-phased walk order"},
         "mask": {"bytes": 1.8263e9,
                  "source": "ncu launch list, 720p, pool + pooled_map + select kernels"},
     }

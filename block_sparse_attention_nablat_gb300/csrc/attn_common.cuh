@@ -20,7 +20,7 @@ struct UnitInfo {
   uint32_t a[kMaxWords];  // kept by the first query block of the pair
   uint32_t b[kMaxWords];  // kept by the second
   int n;                  // union size
-  int pad;
+  int start;              // first key block of the walk (the walk wraps around)
 };
 
 struct Cursor {
@@ -36,7 +36,8 @@ constexpr int kMaxEntries = 32 * kMaxWords;  // entries of a unit (s1 <= 2048)
 // 2l and 2l + 1, starting where the lanes before it end.  Lets the threads
 // that walk a unit's entries read one byte per entry instead of each
 // scanning the bitmaps.
-__device__ __forceinline__ int list_entries(const UnitInfo &inf, uint8_t *fl, int lane) {
+__device__ __forceinline__ int list_entries(const UnitInfo &inf, uint8_t *fl, int lane,
+                                            int start = 0) {
   static_assert(kMaxWords == 64, "two bitmap words per lane");
   const uint32_t u0 = inf.a[2 * lane] | inf.b[2 * lane];
   const uint32_t u1 = inf.a[2 * lane + 1] | inf.b[2 * lane + 1];
@@ -48,16 +49,45 @@ __device__ __forceinline__ int list_entries(const UnitInfo &inf, uint8_t *fl, in
     if (lane >= o) incl += y;
   }
   int pos = incl - mine;
+  const int n = __shfl_sync(0xffffffffu, incl, 31);
+  // entries below `start` go last: r0 of them, so entry e is walked at (e - r0) mod n
+  const int w0 = start >> 5;
+  auto below = [&](int w, uint32_t u) -> int {
+    return w < w0 ? __popc(u) : w == w0 ? __popc(u & ((1u << (start & 31)) - 1u)) : 0;
+  };
+  const int r0 = __reduce_add_sync(0xffffffffu, (unsigned)(below(2 * lane, u0) +
+                                                           below(2 * lane + 1, u1)));
 #pragma unroll
   for (int hw = 0; hw < 2; ++hw) {
     const int w = 2 * lane + hw;
     const uint32_t aw = inf.a[w], bw = inf.b[w];
     for (uint32_t m = hw ? u1 : u0; m; m &= m - 1u) {
       const int bit = __ffs(m) - 1;
-      fl[pos++] = (uint8_t)(((aw >> bit) & 1u) | (((bw >> bit) & 1u) << 1));
+      const int at = pos >= r0 ? pos - r0 : pos - r0 + n;
+      fl[at] = (uint8_t)(((aw >> bit) & 1u) | (((bw >> bit) & 1u) << 1));
+      ++pos;
     }
   }
-  return __shfl_sync(0xffffffffu, incl, 31);
+  return n;
+}
+
+// A cursor over the unit's entries that starts at key block `start` and wraps
+// around: the walk order list_entries writes for the same start.
+__device__ __forceinline__ Cursor cursor_at(const UnitInfo &inf, int start) {
+  const int w0 = start >> 5;
+  return Cursor{w0, (inf.a[w0] | inf.b[w0]) & (~0u << (start & 31))};
+}
+// Next entry of a cursor_at walk; called at most n times per unit.
+__device__ __forceinline__ int next_entry_wrap(const UnitInfo &inf, Cursor &c, int start) {
+  const int w0 = start >> 5;
+  for (int i = 0; c.m == 0u && i <= kMaxWords; ++i) {
+    c.w = c.w + 1 == kMaxWords ? 0 : c.w + 1;
+    c.m = inf.a[c.w] | inf.b[c.w];
+    if (c.w == w0) c.m &= (1u << (start & 31)) - 1u;  // back at the start word
+  }
+  const int bit = c.m ? __ffs(c.m) - 1 : 0;
+  c.m &= c.m - 1u;
+  return c.w * 32 + bit;
 }
 
 __device__ __forceinline__ int next_entry(const UnitInfo &inf, Cursor &c, uint32_t &flags) {
@@ -142,11 +172,11 @@ struct StrideScratch {
   uint32_t bits[12][kMaxWords];
   unsigned long long total[kMaxCands];
   int cand[kMaxCands];
-  int ncand, chosen;
+  int ncand, chosen, mean_union;
 };
 
 template <class L>
-__device__ int choose_pair_stride(const L &P, StrideScratch *sc) {
+__device__ int choose_pair_stride(const L &P, StrideScratch *sc, int *mean_union = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
@@ -160,7 +190,7 @@ __device__ int choose_pair_stride(const L &P, StrideScratch *sc) {
   }
   __syncthreads();
   const int ncand = sc->ncand;
-  if (ncand > 1) {
+  if (ncand > 1 || mean_union) {
     // at most 12 warps take part (one scratch row each); the others skip to the barrier
     const int nw = (int)(blockDim.x >> 5) < 12 ? (int)(blockDim.x >> 5) : 12;
     uint32_t *bits = sc->bits[warp < 12 ? warp : 0];
@@ -206,9 +236,12 @@ __device__ int choose_pair_stride(const L &P, StrideScratch *sc) {
     for (int c = 1; c < ncand; ++c)
       if (sc->total[c] < sc->total[best]) best = c;
     sc->chosen = sc->cand[best];
+    const unsigned long long m = sc->total[best] / kSamples;
+    sc->mean_union = m > 0 ? (int)m : 1;
   }
   __syncthreads();
   const int d = sc->chosen;
+  if (mean_union) *mean_union = sc->mean_union;
   __syncthreads();  // the scratch is handed back to the pipeline after this
   return d;
 }

@@ -18,7 +18,13 @@
 //    shares more of its kept list than the horizontal one (d = 1), so fewer
 //    MMAs are spent on entries only one block of the pair needs.  Persistent
 //    CTAs (one per SM) take units round-robin in head-major order, so
-//    co-running CTAs share one head's K/V in L2.
+//    co-running CTAs share one head's K/V in L2.  A unit's walk over its
+//    entries starts at the key block where a sweep of s1 blocks per mean unit
+//    would be after the entries its CTA has walked so far, and wraps around:
+//    units of different lengths leave the CTAs at different points of their
+//    lists, and this puts the CTAs of a head back in step (a head's K and V,
+//    50 MB at 720p, do not stay in L2 across the staggered sweeps).  The order
+//    depends on the lists alone, so results are reproducible bit for bit.
 //  * A step covers two KV entries (128 keys).  Measured on this hardware, a
 //    bf16 tcgen05 MMA with M = 128, K = 16 takes 48 cycles at N = 64 (two
 //    thirds of the tensor rate) and N / 2 cycles from N = 128 up (the full
@@ -142,6 +148,7 @@ struct Params {
   float scale_log2;
   int *status;
   int pstride;  // query blocks i and i + pstride form a pair (set in the kernel)
+  int mean_union;  // mean union size of the sampled pairs (set in the kernel)
 };
 
 
@@ -236,6 +243,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
   const int s1 = P.S >> 6, npairs = (s1 + 1) >> 1;
   const long units = (long)P.B * P.h * npairs;
   uint32_t gk = 0, kq = 0;  // K pair slots issued, Q tiles issued
+  uint64_t tau = 0;         // entries walked by this CTA, plus a per-unit allowance
   bool stop = false;  // lane 0: a wait gave up; every lane leaves together at the loop top
   int k = 0;
   for (long u = blockIdx.x; u < units; u += gridDim.x, ++k) {
@@ -280,9 +288,21 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
     }
     if (bad) atomicCAS(P.status, kDevOk, kDevBadIndex);
     __syncwarp();
+    // The walk starts at the key block where a sweep of s1 blocks per mean unit
+    // would be after the entries this CTA has walked so far (its units' lengths
+    // plus a per-unit allowance), and wraps around.  CTAs walk entries at about
+    // the same pace, so the CTAs on a head reach the same K/V tiles at about the
+    // same time and share them in L2, while the order stays a function of the
+    // lists alone (the result is reproducible bit for bit).
+    const int mu = P.mean_union;
+    const int start = (int)(((tau % (uint64_t)mu) * (uint64_t)s1) / (uint64_t)mu);
     // entry count, and the entries' membership bits for the softmax warps
-    const int cnt = list_entries(inf, smem + C::kOffFlags + ub * kMaxEntries, lane);
-    if (lane == 0) inf.n = cnt;
+    const int cnt = list_entries(inf, smem + C::kOffFlags + ub * kMaxEntries, lane, start);
+    if (lane == 0) {
+      inf.n = cnt;
+      inf.start = start;
+    }
+    tau += (uint64_t)cnt + (cnt > 0 ? 8u : 1u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar.info_full[ub]);
     if (lane != 0 || cnt == 0) continue;
@@ -300,7 +320,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
                     un.hh, pair_block(un.pr, side, P.pstride) * 64, un.b);
     ++kq;
     const int steps = (cnt + 1) >> 1;
-    Cursor ck{0, inf.a[0] | inf.b[0]};
+    Cursor ck = cursor_at(inf, start);
     bool go = true;
     auto load_k = [&](int s) {  // both entries of step s into one pair slot
       // pair slot gk % 3 is free once the QK^T of step gk - 3 is done, which is
@@ -314,8 +334,7 @@ __device__ void producer(const Params &P, const CUtensorMap *tmQ, const CUtensor
       mbar_expect_tx(&bar.k_full[ks], ne * C::kTileBytes);
       uint8_t *slot = smem + C::kOffK + ks * C::kPairBytes;
       for (int x = 0; x < ne; ++x) {
-        uint32_t fl;
-        const int j = next_entry(inf, ck, fl);
+        const int j = next_entry_wrap(inf, ck, start);
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(slot + c * C::kPairBox + x * 64 * 128, tmK, &bar.k_full[ks], c * 64, un.hh,
@@ -355,7 +374,8 @@ __device__ void v_producer(const Params &P, const CUtensorMap *tmV, uint8_t *sme
     const UnitInfo &inf = info[ub];
     const int n = inf.n;
     const Unit un = decode(u, npairs, P.h);
-    Cursor cv{0, inf.a[0] | inf.b[0]};
+    const int start = inf.start;
+    Cursor cv = cursor_at(inf, start);
     for (int e = 0; e < n && go; e += 2) {
       const uint32_t vp = gv % C::kVPairs;
       if (gv >= (uint32_t)C::kVPairs) {
@@ -367,8 +387,7 @@ __device__ void v_producer(const Params &P, const CUtensorMap *tmV, uint8_t *sme
       const int ne = e + 1 < n ? 2 : 1;
       mbar_expect_tx(&bar.v_full[vp], ne * C::kTileBytes);
       for (int x = 0; x < ne; ++x) {
-        uint32_t fl;
-        const int j = next_entry(inf, cv, fl);
+        const int j = next_entry_wrap(inf, cv, start);
 #pragma unroll
         for (int c = 0; c < C::kBoxes; ++c)
           tma_load_4d(smem + C::kOffV + (vp * 2 + x) * C::kTileBytes + c * 64 * 128, tmV,
@@ -737,7 +756,8 @@ __global__ void __launch_bounds__(384, 1)
   // the K / V staging area is free until the producer starts
   static_assert(sizeof(StrideScratch) <= (size_t)C::kOffInfo - C::kOffK, "stride scratch fits");
   Params Pp = P;
-  Pp.pstride = choose_pair_stride(P, reinterpret_cast<StrideScratch *>(smem + C::kOffK));
+  Pp.pstride = choose_pair_stride(P, reinterpret_cast<StrideScratch *>(smem + C::kOffK),
+                                  &Pp.mean_union);
 
   if (warp == 0) {
     producer<D>(Pp, &tmQ, &tmK, &tmV, smem, info, bar, abort);
