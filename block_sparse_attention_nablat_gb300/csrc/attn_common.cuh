@@ -32,7 +32,8 @@ constexpr int kMaxEntries = 32 * kMaxWords;  // entries of a unit (s1 <= 2048)
 
 // Warp-wide: the unit's entry count, and each entry's two membership bits
 // (bit 0: first block of the pair, bit 1: second) written to fl[0 .. n) in
-// entry order (ascending key block).  Lane l lists the entries of bitmap words
+// walk order: ascending key block from block `start`, then around from block 0
+// (start = 0: plain ascending order).  Lane l lists the entries of bitmap words
 // 2l and 2l + 1, starting where the lanes before it end.  Lets the threads
 // that walk a unit's entries read one byte per entry instead of each
 // scanning the bitmaps.
@@ -166,7 +167,9 @@ struct Ring {
 // pairs have the smallest total list union over a fixed sample of pairs.  Run
 // by all threads of every CTA (the first 12 warps do the counting) on scratch shared memory
 // before the roles start; integer counts make the choice identical in every
-// CTA.  L: any struct with B, S, h and the CSR lists kv_nb, kv_inds.
+// CTA.  L: any struct with B, S, h and the CSR lists kv_nb, kv_inds.  With
+// mean_union given, the sample is counted even when d = 1 is the only
+// candidate, and *mean_union receives the chosen d's mean union size (>= 1).
 constexpr int kMaxCands = 24, kSamples = 16;
 struct StrideScratch {
   uint32_t bits[12][kMaxWords];
