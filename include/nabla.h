@@ -202,6 +202,10 @@ nabla_status nabla_build_mask_topk(const void *q, const void *k, nabla_dtype dt,
  * bf16: QK^T and PV run on the tcgen05 tensor cores (bf16 operands, fp32
  * accumulators; P is rounded to bf16 before PV); o is written as bf16.
  * f32: fp32 CUDA-core arithmetic throughout; o is written as fp32.
+ * Results are reproducible bit for bit: on a given GPU model, repeated calls on
+ * the same inputs give the same o (and lse).  The order in which a row's kept
+ * blocks are accumulated depends only on kv_nb, kv_inds and the number of SMs,
+ * never on timing.
  *
  *   q, k, v, o  [B, S, h, D] device, element type dt; o is overwritten.
  *   kv_nb       [B, h, s1] device int32, each in [0, s1].
